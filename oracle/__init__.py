@@ -1,0 +1,218 @@
+"""CPU oracle for the FP8 fine-grained-scaled GEMM (NT layout, bf16 output).
+
+TEST INFRASTRUCTURE ONLY.  Only `tests/`, `__graft_entry__.smoke()` and the
+CPU-baseline leg of `bench.py` may import this package.  It shares no code with
+the CUDA path and never imports it; the two meet only through the seeded inputs
+of `workloads`.
+
+The arithmetic lives in `ref_gemm.c` (plain C, double precision, one bf16
+rounding at the end); this module loads it with ctypes and marshals numpy
+arrays.  See `ref_gemm.c` for the formula and the pages it follows
+(DeepGEMM, es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
+layout" and "Dense y Grouped GEMM").
+
+Every function takes and returns numpy arrays:
+  A, B          uint8 e4m3 codes, row-major ([M,K] / [N,K], grouped [G,...,K])
+  sa            float32, K-group-major: [kb, ld_sa] (masked: [G, kb, ld_sa])
+  sb            float32, [nb, kb] (grouped: [G, nb, kb])
+  D (returned)  uint16 bf16 bit patterns
+
+Parity status of each function (what pins it, in tests/test_oracle_pins.py):
+  e4m3_to_double   pinned: all 256 codes vs the format definition and torch
+  bf16_rne         pinned: brute-force neighbour search, constructed ties,
+                   double-rounding traps, torch's fp32->bf16 on fp32 inputs
+  gemm_nt          pinned: exact rational brute force, exact integer results,
+                   identity, linearity/transpose, float64 library closed form
+  grouped_*        pinned: equal to per-expert / per-group dense runs,
+                   padding rows +0 and masked rows untouched (bit-exact)
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIBS = {}
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_int = ctypes.c_int
+
+
+def _load(path):
+    lib = ctypes.CDLL(path)
+    lib.dg_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.dg_ref_e4m3_to_double.restype = ctypes.c_double
+    lib.dg_ref_bf16_rne.argtypes = [ctypes.c_double]
+    lib.dg_ref_bf16_rne.restype = ctypes.c_uint16
+    lib.dg_ref_max_threads.argtypes = []
+    lib.dg_ref_max_threads.restype = _int
+    lib.dg_ref_gemm_nt_f64.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _f64p, _int, _int, _int, _int]
+    lib.dg_ref_gemm_nt.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _u16p, _int, _int, _int, _int]
+    lib.dg_ref_gemm_nt_rows.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _u16p, _int, _int,
+                                        _i64p, _int, _int]
+    lib.dg_ref_grouped_contiguous_rows.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _i32p,
+                                                   _u16p, _int, _int, _int, _i64p, _int, _int]
+    lib.dg_ref_grouped_masked.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _i32p, _u16p,
+                                          _int, _int, _int, _int, _int]
+    for f in ("dg_ref_gemm_nt_f64", "dg_ref_gemm_nt", "dg_ref_gemm_nt_rows",
+              "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked"):
+        getattr(lib, f).restype = None
+    return lib
+
+
+def lib(path=None):
+    """The oracle library (built on first use); `path` selects another build
+    of the same source (the test-only mutants)."""
+    if path is None:
+        path = _build.build()
+    if path not in _LIBS:
+        _LIBS[path] = _load(path)
+    return _LIBS[path]
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a, ptype):
+    return a.ctypes.data_as(ptype)
+
+
+class Oracle:
+    """Bound view of one oracle build (the normal one unless `path` is given)."""
+
+    def __init__(self, path=None):
+        self.lib = lib(path)
+
+    # -- scalar pieces ----------------------------------------------------
+    def e4m3_to_double(self, code):
+        return self.lib.dg_ref_e4m3_to_double(int(code) & 0xFF)
+
+    def bf16_rne(self, x):
+        return int(self.lib.dg_ref_bf16_rne(float(x)))
+
+    def max_threads(self):
+        return int(self.lib.dg_ref_max_threads())
+
+    # -- dense ------------------------------------------------------------
+    def gemm_nt_f64(self, A, sa, B, sb, nthreads=0):
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        M, K = A.shape
+        N = B.shape[0]
+        acc = np.zeros((M, N), np.float64)
+        self.lib.dg_ref_gemm_nt_f64(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                    _p(sb, _f32p), _p(acc, _f64p), M, N, K, nthreads)
+        return acc
+
+    def gemm_nt(self, A, sa, B, sb, nthreads=0):
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        M, K = A.shape
+        N = B.shape[0]
+        _check_dense(A, sa, B, sb)
+        D = np.zeros((M, N), np.uint16)
+        self.lib.dg_ref_gemm_nt(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                _p(sb, _f32p), _p(D, _u16p), M, N, K, nthreads)
+        return D
+
+    def gemm_nt_rows(self, A, sa, B, sb, rows, nthreads=0):
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        rows = _c(rows, np.int64)
+        M, K = A.shape
+        N = B.shape[0]
+        _check_dense(A, sa, B, sb)
+        assert rows.size == 0 or (rows.min() >= 0 and rows.max() < M)
+        D = np.zeros((rows.size, N), np.uint16)
+        self.lib.dg_ref_gemm_nt_rows(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                     _p(sb, _f32p), _p(D, _u16p), N, K, _p(rows, _i64p),
+                                     rows.size, nthreads)
+        return D
+
+    # -- grouped ----------------------------------------------------------
+    def grouped_contiguous(self, A, sa, B, sb, m_indices, rows=None, nthreads=0):
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        m_indices = _c(m_indices, np.int32)
+        M, K = A.shape
+        G, N, K2 = B.shape
+        assert K2 == K and m_indices.shape == (M,)
+        assert sa.shape[0] == K // 128 and sa.shape[1] >= M
+        assert sb.shape == (G, (N + 127) // 128, K // 128)
+        if rows is None:
+            rows_p, nrows = None, M
+        else:
+            rows = _c(rows, np.int64)
+            assert rows.size == 0 or (rows.min() >= 0 and rows.max() < M)
+            rows_p, nrows = _p(rows, _i64p), rows.size
+        D = np.zeros((nrows, N), np.uint16)
+        self.lib.dg_ref_grouped_contiguous_rows(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1],
+                                                _p(B, _u8p), _p(sb, _f32p),
+                                                _p(m_indices, _i32p), _p(D, _u16p), N, K, G,
+                                                rows_p, nrows, nthreads)
+        return D
+
+    def grouped_masked(self, A, sa, B, sb, masked_m, D_init, nthreads=0):
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        masked_m = _c(masked_m, np.int32)
+        G, max_m, K = A.shape
+        G2, N, K2 = B.shape
+        assert G2 == G and K2 == K and masked_m.shape == (G,)
+        assert sa.shape[:2] == (G, K // 128) and sa.shape[2] >= max_m
+        assert sb.shape == (G, (N + 127) // 128, K // 128)
+        assert masked_m.min() >= 0 and masked_m.max() <= max_m
+        D = np.array(D_init, dtype=np.uint16, copy=True, order="C")
+        assert D.shape == (G, max_m, N)
+        self.lib.dg_ref_grouped_masked(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                       _p(sb, _f32p), _p(masked_m, _i32p), _p(D, _u16p),
+                                       G, max_m, N, K, nthreads)
+        return D
+
+
+def _check_dense(A, sa, B, sb):
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2 and K % 128 == 0
+    assert sa.ndim == 2 and sa.shape[0] == K // 128 and sa.shape[1] >= M
+    assert sb.shape == ((N + 127) // 128, K // 128)
+
+
+_default = None
+
+
+def default():
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def bf16_bits_to_float(bits):
+    """uint16 bf16 bit patterns -> float32 values (exact)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def gemm_nt(*a, **k):
+    return default().gemm_nt(*a, **k)
+
+
+def gemm_nt_rows(*a, **k):
+    return default().gemm_nt_rows(*a, **k)
+
+
+def grouped_contiguous(*a, **k):
+    return default().grouped_contiguous(*a, **k)
+
+
+def grouped_masked(*a, **k):
+    return default().grouped_masked(*a, **k)

@@ -1,0 +1,313 @@
+/*
+ * CPU oracle for the FP8 fine-grained-scaled GEMM (NT layout, bf16 output).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this code.  It shares nothing with the CUDA path:
+ * no headers, helpers, tables or constants.  It is plain and slow on purpose,
+ * so that a reader can check it against the method's definition by eye.
+ *
+ * What it computes (DeepGEMM: "clean and efficient FP8 GEMM kernels with
+ * fine-grained scaling", es.news.hada.io/topic?id=19459, section
+ * "Interfaz GEMM y restricciones de layout"; DeepSeek-V3 fine-grained scaling
+ * as summarised on es.news.hada.io/topic?id=19444, first list):
+ *
+ *   D[m,n] = bf16_rne( sum over K groups g of
+ *              ( sum_{k in g} dec(A[m,k]) * dec(B[n,k]) ) * sa[m,g] * sb[n/128,g] )
+ *
+ *   A  : e4m3 codes, [M][K] row-major (the non-transposed LHS of "NT")
+ *   B  : e4m3 codes, [N][K] row-major (the transposed RHS of "NT")
+ *   g  : a 128-wide slice of K
+ *   sa : fp32, one per (row, K group), stored K-group-major ("transposed",
+ *        TMA-aligned): sa[g * ld_sa + m]
+ *   sb : fp32, one per 128x128 block of B: sb[(n/128) * kb + g]
+ *   D  : bf16 bit patterns, [M][N] row-major
+ *
+ * Arithmetic: each group's dot product is summed in double, which is exact
+ * (every product of two e4m3 values is a multiple of 2^-18 below 2^18, and
+ * 128 of them fit in 53 bits).  The scale products and the sum over groups
+ * round in double (relative error ~1e-16).  The result is rounded once, from
+ * double straight to bf16, round-to-nearest-even.
+ *
+ * The M-grouped forms (same pages, section "Dense y Grouped GEMM"):
+ *  - contiguous: rows of all experts are concatenated along M; m_indices[m]
+ *    names the expert of row m, and -1 marks a padding row, whose output is
+ *    written as +0;
+ *  - masked: A is [G][max_m][K]; only the first masked_m[g] rows of group g
+ *    are computed; the other output rows are left as they were.
+ *
+ * Build: gcc -O2 -fopenmp -shared -fPIC ref_gemm.c -o libdgref.so -lm
+ * (oracle/build.py does this).  OpenMP only splits rows across threads; the
+ * arithmetic of every output element is the same with any thread count.
+ *
+ * DG_REF_MUTANT (test-only): when defined to a nonzero value, one deliberate
+ * mistake is compiled in, so that the pin tests can show they catch it.  The
+ * normal build never defines it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef DG_REF_MUTANT
+#define DG_REF_MUTANT 0
+#endif
+
+/* ---------------------------------------------------------------- e4m3 -- */
+/* OCP FP8 E4M3 ("fn" variant): 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits.  Exponent field 0 holds subnormals (f/8 * 2^-6).  There is
+ * no infinity; S.1111.111 is NaN, so the largest finite value is 448. */
+double dg_ref_e4m3_to_double(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int f = code & 0x7;
+    double mag;
+    if (e == 0xF && f == 0x7)
+        return NAN;
+#if DG_REF_MUTANT == 4
+    if (e == 0)
+        mag = 0.0;                       /* mutant: subnormals flushed */
+    else
+#else
+    if (e == 0)
+        mag = ldexp((double)f / 8.0, -6); /* subnormal */
+    else
+#endif
+        mag = ldexp(1.0 + (double)f / 8.0, e - 7);
+#if DG_REF_MUTANT == 7
+    (void)sign;
+    return mag;                          /* mutant: sign dropped */
+#else
+    return sign ? -mag : mag;
+#endif
+}
+
+/* ---------------------------------------------------------------- bf16 -- */
+/* bf16: 1 sign bit, 8 exponent bits (bias 127, as fp32), 7 stored mantissa
+ * bits.  Normal values are (1 + f/128) * 2^(e-127); below 2^-126 the spacing
+ * stays 2^-133 (subnormals).  The rounding is to nearest, ties to even, done
+ * once from the double value.  Every bf16 value is also an fp32 value, so the
+ * rounded number is built as a float and its upper 16 bits are returned. */
+uint16_t dg_ref_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    double q; /* spacing of bf16 values around a */
+    if (a == 0.0 || isinf(a)) {
+        float f = (float)x;
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        return (uint16_t)(u >> 16);
+    }
+    if (a < ldexp(1.0, -126)) {
+        q = ldexp(1.0, -133);
+    } else {
+        int ex;
+        frexp(a, &ex);                   /* a = fr * 2^ex with fr in [0.5, 1) */
+        q = ldexp(1.0, (ex - 1) - 7);    /* 8 significant bits */
+    }
+    double r = a / q;                    /* exact: q is a power of two */
+#if DG_REF_MUTANT == 5
+    double n = floor(r);                 /* mutant: truncation instead of RNE */
+#else
+    double n = nearbyint(r);             /* default mode: nearest, ties to even */
+#endif
+    double v = n * q;                    /* exact */
+    float f = (float)v;                  /* exact, or +inf past the bf16 range */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint16_t h = (uint16_t)(u >> 16);
+    if (neg)
+        h |= 0x8000;
+    return h;
+}
+
+/* ------------------------------------------------------- one output row -- */
+/* Computes row m of A (row pointer a_row) against all N rows of B (b_base) and
+ * returns the unrounded double accumulators in acc[N]. */
+static void ref_row_f64(const uint8_t *a_row, const float *sa, int ld_sa, int m,
+                        const uint8_t *b_base, const float *sb,
+                        int N, int K, double *acc)
+{
+    int kb = K / 128;
+    int ng = kb;
+#if DG_REF_MUTANT == 1
+    ng = kb - 1;                          /* mutant: last K group dropped */
+#endif
+    for (int n = 0; n < N; ++n) {
+        const uint8_t *b_row = b_base + (size_t)n * K;
+        double total = 0.0;
+        for (int g = 0; g < ng; ++g) {
+            double dot = 0.0;
+            for (int k = 128 * g; k < 128 * g + 128; ++k) {
+#if DG_REF_MUTANT == 6
+                /* mutant: B read as if it were stored [K][N] */
+                double bv = dg_ref_e4m3_to_double(b_base[(size_t)k * N + n]);
+                (void)b_row;
+#else
+                double bv = dg_ref_e4m3_to_double(b_row[k]);
+#endif
+                dot += dg_ref_e4m3_to_double(a_row[k]) * bv;
+            }
+#if DG_REF_MUTANT == 3
+            double s_a = (double)sa[(size_t)m * kb + g];   /* mutant: sa read row-major */
+#else
+            double s_a = (double)sa[(size_t)g * ld_sa + m];
+#endif
+#if DG_REF_MUTANT == 2
+            double s_b = (double)sb[(size_t)g * ((N + 127) / 128) + n / 128]; /* mutant: sb transposed */
+#else
+            double s_b = (double)sb[(size_t)(n / 128) * kb + g];
+#endif
+#if DG_REF_MUTANT == 8
+            total += dot * s_a;                  /* mutant: B scale dropped */
+            (void)s_b;
+#else
+            total += dot * s_a * s_b;
+#endif
+        }
+        acc[n] = total;
+    }
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int dg_ref_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* -------------------------------------------------------------- dense ---- */
+/* Unrounded accumulators, [M][N] doubles.  Used by the pins that compare the
+ * oracle with a library closed form before the final rounding. */
+void dg_ref_gemm_nt_f64(const uint8_t *A, const float *sa, int ld_sa,
+                        const uint8_t *B, const float *sb,
+                        double *acc, int M, int N, int K, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; ++m)
+        ref_row_f64(A + (size_t)m * K, sa, ld_sa, m, B, sb, N, K,
+                    acc + (size_t)m * N);
+}
+
+/* Rows rows[0..nrows-1] of the dense product, written to D[i][N] (row i of D
+ * holds output row rows[i]). */
+void dg_ref_gemm_nt_rows(const uint8_t *A, const float *sa, int ld_sa,
+                         const uint8_t *B, const float *sb,
+                         uint16_t *D, int N, int K,
+                         const int64_t *rows, int nrows, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; ++i) {
+        int m = (int)rows[i];
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        ref_row_f64(A + (size_t)m * K, sa, ld_sa, m, B, sb, N, K, acc);
+        for (int n = 0; n < N; ++n)
+            D[(size_t)i * N + n] = dg_ref_bf16_rne(acc[n]);
+        free(acc);
+    }
+}
+
+void dg_ref_gemm_nt(const uint8_t *A, const float *sa, int ld_sa,
+                    const uint8_t *B, const float *sb,
+                    uint16_t *D, int M, int N, int K, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; ++m) {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        ref_row_f64(A + (size_t)m * K, sa, ld_sa, m, B, sb, N, K, acc);
+        for (int n = 0; n < N; ++n)
+            D[(size_t)m * N + n] = dg_ref_bf16_rne(acc[n]);
+        free(acc);
+    }
+}
+
+/* ------------------------------------------------- grouped, contiguous --- */
+/* A: [M_total][K]; B: [G][N][K]; sa: [kb][ld_sa]; sb: [G][nb][kb];
+ * m_indices: [M_total], expert of each row or -1 (padding -> +0).
+ * Computes the rows listed in rows[] (all rows when rows == NULL, nrows ==
+ * M_total) into D[i][N]. */
+void dg_ref_grouped_contiguous_rows(const uint8_t *A, const float *sa, int ld_sa,
+                                    const uint8_t *B, const float *sb,
+                                    const int32_t *m_indices,
+                                    uint16_t *D, int N, int K, int num_groups,
+                                    const int64_t *rows, int nrows, int nthreads)
+{
+    int kb = K / 128;
+    int nb = (N + 127) / 128;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; ++i) {
+        int m = rows ? (int)rows[i] : i;
+        int e = m_indices[m];
+        uint16_t *drow = D + (size_t)i * N;
+#if DG_REF_MUTANT == 9
+        if (e < 0) e = 0;                 /* mutant: padding rows computed */
+#endif
+        if (e < 0 || e >= num_groups) {
+            for (int n = 0; n < N; ++n)
+                drow[n] = 0x0000;         /* +0 */
+            continue;
+        }
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        ref_row_f64(A + (size_t)m * K, sa, ld_sa, m,
+                    B + (size_t)e * N * K, sb + (size_t)e * nb * kb, N, K, acc);
+        for (int n = 0; n < N; ++n)
+            drow[n] = dg_ref_bf16_rne(acc[n]);
+        free(acc);
+    }
+}
+
+/* --------------------------------------------------- grouped, masked ----- */
+/* A: [G][max_m][K]; B: [G][N][K]; sa: [G][kb][ld_sa]; sb: [G][nb][kb];
+ * D: [G][max_m][N], updated in place: rows m < masked_m[g] are computed, the
+ * others keep whatever D held. */
+void dg_ref_grouped_masked(const uint8_t *A, const float *sa, int ld_sa,
+                           const uint8_t *B, const float *sb,
+                           const int32_t *masked_m,
+                           uint16_t *D, int num_groups, int max_m, int N, int K,
+                           int nthreads)
+{
+    int kb = K / 128;
+    int nb = (N + 127) / 128;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int g = 0; g < num_groups; ++g) {
+        for (int m = 0; m < max_m; ++m) {
+            int valid = masked_m[g];
+#if DG_REF_MUTANT == 10
+            valid = max_m;                /* mutant: mask ignored */
+#endif
+            if (m >= valid)
+                continue;
+            double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+            ref_row_f64(A + ((size_t)g * max_m + m) * K,
+                        sa + (size_t)g * kb * ld_sa, ld_sa, m,
+                        B + (size_t)g * N * K, sb + (size_t)g * nb * kb, N, K, acc);
+            uint16_t *drow = D + ((size_t)g * max_m + m) * N;
+            for (int n = 0; n < N; ++n)
+                drow[n] = dg_ref_bf16_rne(acc[n]);
+            free(acc);
+        }
+    }
+}

@@ -1,0 +1,370 @@
+"""Checks that pin the CPU oracle to something other than itself.
+
+Each `check_*` function takes an `oracle.Oracle` (the normal build, or a
+test-only mutant with one planted mistake) and raises AssertionError when the
+oracle disagrees with an independent ground truth:
+
+  * the e4m3 and bf16 format definitions (golden fixtures under tests/golden),
+  * torch's own float8_e4m3fn -> float64 and float32 -> bfloat16 conversions,
+  * a brute-force bf16 rounding that searches the sorted table of all bf16
+    values with exact rational arithmetic,
+  * exact rational (integer) evaluation of the GEMM written per K element
+    (sum_k a*b*sa*sb, no grouping), a different form of the same definition,
+  * exact integer results, identity rows, linearity and transposition,
+  * a float64 closed form built from torch.matmul on pre-scaled operands,
+  * grouped results equal to per-expert / per-group dense runs, with padding
+    rows +0 and masked rows untouched, bit for bit.
+
+The GEMM definition these follow: DeepGEMM (es.news.hada.io/topic?id=19459),
+"Interfaz GEMM y restricciones de layout" and "Dense y Grouped GEMM".
+"""
+import bisect
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------ ground truth --
+def torch_e4m3_values():
+    """All 256 e4m3 codes decoded by torch (float64)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+_BF16_POS = None
+
+
+def _bf16_table():
+    """Sorted exact values of all finite non-negative bf16 patterns 0x0000..0x7F7F."""
+    global _BF16_POS
+    if _BF16_POS is None:
+        pats = torch.arange(0, 0x7F80, dtype=torch.int32).to(torch.int16)
+        _BF16_POS = pats.view(torch.bfloat16).to(torch.float64).tolist()
+    return _BF16_POS
+
+
+def bf16_bruteforce(x):
+    """Round x (float or Fraction) to bf16 bits by searching all bf16 values.
+
+    Nearest value wins; at an exact tie the even bit pattern wins; past the
+    largest finite value the result is inf when x is at least half a spacing
+    beyond it (IEEE roundTiesToEven)."""
+    if isinstance(x, float):
+        if x != x:
+            return 0x7FC0
+        if x in (float("inf"), float("-inf")):
+            return 0x7F80 if x > 0 else 0xFF80
+        neg = np.signbit(x)
+        ax = Fraction(abs(x))
+    else:
+        neg = x < 0
+        ax = abs(x)
+    tab = _bf16_table()
+    top = Fraction(tab[-1])
+    half_ulp_top = Fraction(2) ** 119
+    if ax >= top + half_ulp_top:
+        pat = 0x7F80
+    elif ax >= top:
+        pat = 0x7F7F
+    else:
+        i = bisect.bisect_left(tab, float(ax))
+        # candidates around ax (float(ax) may be rounded; check neighbours exactly)
+        cands = [j for j in (i - 2, i - 1, i, i + 1) if 0 <= j < len(tab)]
+        best = None
+        for j in cands:
+            d = abs(Fraction(tab[j]) - ax)
+            key = (d, j & 1)
+            if best is None or key < best[0]:
+                best = (key, j)
+        pat = best[1]
+    return pat | (0x8000 if neg else 0)
+
+
+def e4m3_exact(codes):
+    """Exact value of each code as a Fraction (via torch's decode, which is
+    exact in float64)."""
+    vals = torch_e4m3_values()
+    return [Fraction(float(vals[c])) for c in np.asarray(codes).ravel()]
+
+
+def gemm_exact_bits(A, sa, B, sb):
+    """Exact GEMM by rational arithmetic, written per K element:
+    D[m,n] = sum_k a[m,k] * b[n,k] * sa[m, k//128] * sb[n//128, k//128],
+    then the brute-force bf16 rounding."""
+    M, K = A.shape
+    N = B.shape[0]
+    vals = torch_e4m3_values()
+    # every e4m3 value is an integer multiple of 2^-9
+    ai = (np.rint(vals[A.astype(np.int64)] * 512)).astype(np.int64)
+    bi = (np.rint(vals[B.astype(np.int64)] * 512)).astype(np.int64)
+    out = np.zeros((M, N), np.uint16)
+    for m in range(M):
+        for n in range(N):
+            tot = Fraction(0)
+            for k in range(K):
+                p = int(ai[m, k]) * int(bi[n, k])
+                if p:
+                    tot += Fraction(p, 1 << 18) * Fraction(float(sa[k // 128, m])) \
+                        * Fraction(float(sb[n // 128, k // 128]))
+            out[m, n] = bf16_bruteforce(tot)
+    return out
+
+
+def _f(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _pow2_scales(shape, rng, lo=-3, hi=3):
+    return np.ldexp(1.0, rng.integers(lo, hi + 1, size=shape)).astype(np.float32)
+
+
+# ------------------------------------------------------------------ checks --
+def check_e4m3_golden(orc):
+    with open(os.path.join(GOLDEN, "e4m3_values.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            code_s, val_s = line.split()
+            got = orc.e4m3_to_double(int(code_s, 16))
+            if val_s == "nan":
+                assert got != got, (code_s, got)
+            else:
+                want = float.fromhex(val_s) if "p" in val_s else float(val_s)
+                assert got == want and np.signbit(got) == np.signbit(want), (code_s, got, want)
+
+
+def check_e4m3_all_codes(orc):
+    ref = torch_e4m3_values()
+    for c in range(256):
+        got = orc.e4m3_to_double(c)
+        if ref[c] != ref[c]:
+            assert got != got, c
+        else:
+            assert got == ref[c] and np.signbit(got) == np.signbit(ref[c]), (c, got, ref[c])
+
+
+def check_bf16_golden(orc):
+    with open(os.path.join(GOLDEN, "bf16_rounding.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            x_s, bits_s = line.split()[:2]
+            x = float(x_s) if x_s in ("inf", "-inf") else float.fromhex(x_s)
+            got = orc.bf16_rne(x)
+            assert got == int(bits_s, 16), (x_s, hex(got), bits_s)
+
+
+def check_bf16_bruteforce(orc, n=4000, seed=7):
+    rng = np.random.default_rng(seed)
+    # doubles spread over the whole bf16 range, subnormals and overflow included
+    exps = rng.integers(-140, 131, size=n)
+    mant = rng.random(n) + 1.0
+    sign = np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    xs = sign * np.ldexp(mant, exps)
+    # and values sitting exactly on, just above and just below rounding ties
+    base = np.ldexp(rng.integers(128, 256, size=n // 4).astype(np.float64) + 0.5,
+                    rng.integers(-120, 100, size=n // 4))
+    xs = np.concatenate([xs, base, np.nextafter(base, np.inf), np.nextafter(base, -np.inf)])
+    for x in xs.tolist():
+        got = orc.bf16_rne(x)
+        want = bf16_bruteforce(x)
+        assert got == want, (x.hex(), hex(got), hex(want))
+
+
+def check_bf16_vs_torch_float32(orc, n=20000, seed=11):
+    """On fp32 inputs torch's fp32 -> bf16 cast is a single RNE rounding."""
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for x, w in zip(f.astype(np.float64).tolist(), want.tolist()):
+        assert orc.bf16_rne(x) == w, (x, w)
+
+
+def check_gemm_bruteforce(orc, seed=3):
+    """Random codes and random fp32 scales, exact rational ground truth.
+    N = 136 crosses a 128-row B scale block; K = 256 has two K groups."""
+    for (M, N, K) in ((2, 136, 256), (3, 4, 128), (1, 1, 384)):
+        A = W.random_codes((M, K), seed)
+        B = W.random_codes((N, K), seed + 1)
+        rng = np.random.default_rng(seed)
+        sa = np.zeros((K // 128, W.tma_aligned_ld(M)), np.float32)
+        sa[:, :M] = rng.uniform(0.01, 2.0, size=(K // 128, M)).astype(np.float32)
+        sb = rng.uniform(0.01, 2.0, size=((N + 127) // 128, K // 128)).astype(np.float32)
+        got = orc.gemm_nt(A, sa, B, sb)
+        want = gemm_exact_bits(A, sa, B, sb)
+        assert np.array_equal(got, want), (M, N, K, np.argwhere(got != want)[:5])
+
+
+# integer-valued e4m3 codes: 0, +-1 .. +-16 (every integer up to 16 is exact in e4m3)
+def _int_codes():
+    vals = torch_e4m3_values()
+    ints = {}
+    for c in range(256):
+        v = vals[c]
+        if v == v and v == int(v) and abs(v) <= 16 and not (v == 0 and c != 0):
+            ints[int(v)] = c
+    return ints
+
+
+def check_gemm_exact_integers(orc, seed=5):
+    """Integer-valued inputs and power-of-two scales: every partial sum is an
+    exact integer times a power of two, so the result is known exactly."""
+    ints = _int_codes()
+    keys = np.array(sorted(ints))
+    rng = np.random.default_rng(seed)
+    M, N, K = 9, 200, 512
+    av = rng.choice(keys, size=(M, K))
+    bv = rng.choice(keys, size=(N, K))
+    # sparse copy keeps |D| < 256, where bf16 holds every integer
+    av_sp = np.where(rng.random((M, K)) < 0.03, np.clip(av, -2, 2), 0)
+    bv_sp = np.where(rng.random((N, K)) < 0.03, np.clip(bv, -2, 2), 0)
+    for (a_int, b_int, pow2) in ((av, bv, True), (av_sp, bv_sp, False)):
+        A = np.vectorize(ints.get)(a_int).astype(np.uint8)
+        B = np.vectorize(ints.get)(b_int).astype(np.uint8)
+        kb, nb = K // 128, (N + 127) // 128
+        if pow2:
+            sa = np.zeros((kb, W.tma_aligned_ld(M)), np.float32)
+            sa[:, :M] = _pow2_scales((kb, M), rng)
+            sb = _pow2_scales((nb, kb), rng)
+        else:
+            sa = np.ones((kb, W.tma_aligned_ld(M)), np.float32)
+            sb = np.ones((nb, kb), np.float32)
+        got = orc.gemm_nt(A, sa, B, sb)
+        want = np.zeros((M, N), np.uint16)
+        for m in range(M):
+            for n in range(N):
+                tot = Fraction(0)
+                for g in range(kb):
+                    d = int(np.dot(a_int[m, 128 * g:128 * g + 128].astype(np.int64),
+                                   b_int[n, 128 * g:128 * g + 128].astype(np.int64)))
+                    tot += d * Fraction(float(sa[g, m])) * Fraction(float(sb[n // 128, g]))
+                want[m, n] = bf16_bruteforce(tot)
+                if not pow2:
+                    assert abs(tot) < 256 and tot.denominator == 1
+        assert np.array_equal(got, want), np.argwhere(got != want)[:5]
+
+
+def check_gemm_identity(orc, seed=9):
+    """Row m of A is one-hot 1.0 at column k0 with sa = 1, so row m of D is
+    B[:, k0] * sb[n//128, k0//128] rounded once to bf16."""
+    M, N, K = 4, 260, 384
+    B = W.random_codes((N, K), seed)
+    rng = np.random.default_rng(seed)
+    sb = rng.uniform(0.01, 4.0, size=((N + 127) // 128, K // 128)).astype(np.float32)
+    A = np.zeros((M, K), np.uint8)
+    k0s = [0, 129, 255, 383]
+    for m, k0 in enumerate(k0s):
+        A[m, k0] = 0x38  # 1.0
+    sa = np.ones((K // 128, W.tma_aligned_ld(M)), np.float32)
+    got = orc.gemm_nt(A, sa, B, sb)
+    vals = torch_e4m3_values()
+    for m, k0 in enumerate(k0s):
+        for n in range(N):
+            exact = Fraction(float(vals[B[n, k0]])) * Fraction(float(sb[n // 128, k0 // 128]))
+            assert got[m, n] == bf16_bruteforce(exact), (m, n)
+
+
+def check_gemm_linearity_transpose(orc, seed=13):
+    rng = np.random.default_rng(seed)
+    M, N, K = 6, 300, 384
+    A = W.random_codes((M, K), seed)
+    B = W.random_codes((N, K), seed + 1)
+    kb, nb = K // 128, (N + 127) // 128
+    sa = np.zeros((kb, W.tma_aligned_ld(M)), np.float32)
+    sa[:, :M] = rng.uniform(0.5, 2.0, size=(kb, M)).astype(np.float32)
+    sb = rng.uniform(0.5, 2.0, size=(nb, kb)).astype(np.float32)
+    D0 = _f(orc.gemm_nt(A, sa, B, sb))
+    # all groups of row 2 scaled by 2^3 -> row 2 scaled by 2^3 exactly
+    sa2 = sa.copy(); sa2[:, 2] *= 8.0
+    D1 = _f(orc.gemm_nt(A, sa2, B, sb))
+    exp = D0.copy(); exp[2] *= 8.0
+    assert np.array_equal(D1, exp)
+    # all groups of B block 1 scaled by 2^-2 -> columns 128..255 scaled by 2^-2
+    sb2 = sb.copy(); sb2[1, :] *= 0.25
+    D2 = _f(orc.gemm_nt(A, sa, B, sb2))
+    exp = D0.copy(); exp[:, 128:256] *= 0.25
+    assert np.array_equal(D2, exp)
+    # one K group's scales zeroed -> equals the GEMM on that group's zeroed codes
+    sa3 = sa.copy(); sa3[1, :] = 0.0
+    A3 = A.copy(); A3[:, 128:256] = 0
+    assert np.array_equal(orc.gemm_nt(A, sa3, B, sb), orc.gemm_nt(A3, sa, B, sb))
+    # transposition: with 128x128 blocks on both sides and per-group constant
+    # scales, swapping the operands (and their scales) transposes D
+    Mt = Nt = 128
+    At = W.random_codes((Mt, K), seed + 2)
+    Bt = W.random_codes((Nt, K), seed + 3)
+    alpha = rng.uniform(0.5, 2.0, size=kb).astype(np.float32)
+    beta = rng.uniform(0.5, 2.0, size=kb).astype(np.float32)
+    sa_t = np.repeat(alpha[:, None], Mt, axis=1)
+    sb_t = beta[None, :].copy()
+    sa_s = np.repeat(beta[:, None], Nt, axis=1)
+    sb_s = alpha[None, :].copy()
+    D = orc.gemm_nt(At, sa_t, Bt, sb_t)
+    Ds = orc.gemm_nt(Bt, sa_s, At, sb_s)
+    assert np.array_equal(D, Ds.T)
+
+
+def check_gemm_closed_form(orc, seed=17):
+    """float64 torch.matmul on decoded, pre-scaled operands equals the
+    oracle's unrounded accumulators to ~1e-13 relative."""
+    M, N, K = 33, 257, 640
+    p = W.dense_problem(M, N, K, seed)
+    vals = torch.from_numpy(torch_e4m3_values())
+    Ad = vals[torch.from_numpy(p["A"]).long()]
+    Bd = vals[torch.from_numpy(p["B"]).long()]
+    sa_exp = torch.from_numpy(p["sa"][:, :M]).double().T.repeat_interleave(128, dim=1)
+    sb_exp = torch.from_numpy(p["sb"]).double().repeat_interleave(128, dim=0)[:N] \
+        .repeat_interleave(128, dim=1)
+    ref = ((Ad * sa_exp) @ (Bd * sb_exp).T).numpy()
+    mag = (torch.abs(Ad * sa_exp) @ torch.abs(Bd * sb_exp).T).numpy()
+    acc = orc.gemm_nt_f64(p["A"], p["sa"], p["B"], p["sb"])
+    assert np.all(np.abs(acc - ref) <= 1e-13 * mag + 1e-300)
+    bits = orc.gemm_nt(p["A"], p["sa"], p["B"], p["sb"])
+    assert np.array_equal(bits, np.vectorize(bf16_bruteforce, otypes=[np.uint16])(acc))
+
+
+def check_grouped_contiguous(orc, seed=19):
+    p = W.contiguous_problem(3, 136, 256, 1, 200, seed)
+    D = orc.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], p["m_indices"])
+    mi = p["m_indices"]
+    assert np.all(D[mi < 0] == 0)  # +0 bit pattern on padding rows
+    assert (mi < 0).any()
+    for e in range(p["G"]):
+        rows = np.nonzero(mi == e)[0]
+        dense = orc.gemm_nt_rows(p["A"], p["sa"], p["B"][e], p["sb"][e], rows)
+        assert np.array_equal(D[rows], dense), e
+    # a row subset gives the same rows
+    sub = np.array([0, 5, len(mi) - 1, 130], np.int64)
+    assert np.array_equal(orc.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], mi, rows=sub),
+                          D[sub])
+
+
+def check_grouped_masked(orc, seed=23):
+    p = W.masked_problem(3, 200, 136, 256, 60, seed)
+    G, max_m, N = p["G"], p["max_m"], p["N"]
+    init = np.full((G, max_m, N), W.BF16_SENTINEL, np.uint16)
+    D = orc.grouped_masked(p["A"], p["sa"], p["B"], p["sb"], p["masked_m"], init)
+    for g in range(G):
+        v = int(p["masked_m"][g])
+        assert np.all(D[g, v:] == W.BF16_SENTINEL)
+        dense = orc.gemm_nt(p["A"][g], p["sa"][g], p["B"][g], p["sb"][g])
+        assert np.array_equal(D[g, :v], dense[:v]), g
+    assert (p["masked_m"] < max_m).all()
+
+
+ALL_CHECKS = [
+    check_e4m3_golden, check_e4m3_all_codes, check_bf16_golden, check_bf16_bruteforce,
+    check_bf16_vs_torch_float32, check_gemm_bruteforce, check_gemm_exact_integers,
+    check_gemm_identity, check_gemm_linearity_transpose, check_gemm_closed_form,
+    check_grouped_contiguous, check_grouped_masked,
+]
