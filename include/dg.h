@@ -1,0 +1,165 @@
+/*
+ * dg.h - C ABI of the GB300 (sm_103a) FP8 fine-grained-scaled GEMM library.
+ *
+ * Every GEMM entry point computes, for the rows it covers,
+ *
+ *   D[m,n] = bf16( sum over K groups g of (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
+ *
+ * with A e4m3 (OCP "E4M3FN" codes, one byte each), B e4m3, both row-major with
+ * K innermost ("NT": LHS not transposed, RHS transposed), g a 128-wide slice of
+ * K, one fp32 scale per row per K group for A and one fp32 scale per 128x128
+ * block for B, and a bf16 (round-to-nearest-even) output.  This is the GEMM of
+ * DeepGEMM (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
+ * layout"; the names follow the original release as listed on
+ * deepep.org/zh/deepgemm, "接口设计").
+ *
+ * Conventions shared by all entry points
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the library
+ *    keeps no reference after the call returns and allocates nothing.
+ *  - A, B, D and sa must be 16-byte aligned; sb 4-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  A call never synchronises, never reads device memory
+ *    from the host and never allocates, so it can be captured in a CUDA graph.
+ *  - Argument errors are reported by the return value before anything is
+ *    launched; dg_last_error_string() gives the detail.  Errors found on the
+ *    device (a masked_m out of range, a contiguous block that mixes experts, an
+ *    internal wait that timed out) are recorded in a device status word read by
+ *    dg_get_device_status().
+ *  - The current CUDA device must be a compute capability 10.3 GPU (GB300).
+ *
+ * Layouts
+ *  - A  : [M][K] bytes (masked form: [G][max_m][K]).
+ *  - sa : fp32, K-group-major ("transposed", TMA-aligned):
+ *         sa[g * ld_sa + m], g < K/128, ld_sa >= M (masked: max_m), ld_sa % 4 == 0.
+ *         Masked form: sa[(grp * K/128 + g) * ld_sa + m].
+ *  - B  : [N][K] bytes (grouped forms: [G][N][K]).
+ *  - sb : fp32 [ceil(N/128)][K/128] (grouped forms: [G][ceil(N/128)][K/128]);
+ *         sb[(n/128) * (K/128) + g].
+ *  - D  : bf16 bit patterns [M][N] (masked form: [G][max_m][N]).
+ *  - Shape limits: K % 128 == 0, 128 <= K <= 65536; N % 16 == 0; N >= 16.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dg_status {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad group count */
+  DG_ERR_UNSUPPORTED_SHAPE = 2, /* K or N outside the shape limits above */
+  DG_ERR_MISALIGNED = 3,        /* pointer or ld_sa alignment */
+  DG_ERR_NO_DEVICE = 4,         /* no CUDA device available */
+  DG_ERR_ARCH = 5,              /* current device is not compute capability 10.3 */
+  DG_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed */
+  DG_ERR_TIMEOUT = 7,           /* device: an internal wait gave up */
+  DG_ERR_MASK_RANGE = 8,        /* device: masked_m[g] outside [0, max_m] (clamped) */
+  DG_ERR_EXPERT_RANGE = 9       /* device: m_indices outside [-1, G) or a 128-row block mixes experts */
+} dg_status;
+
+/* Dense GEMM (DeepGEMM "gemm_fp8_fp8_bf16_nt", deepep.org/zh/deepgemm, "接口设计").
+ * A [M][K], sa [K/128][ld_sa], B [N][K], sb [ceil(N/128)][K/128], D [M][N].
+ * M == 0 is a no-op. */
+dg_status dg_gemm_fp8_fp8_bf16_nt(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, void* D, int M, int N, int K, void* stream);
+
+/* M-grouped GEMM, contiguous layout (DeepGEMM "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous";
+ * es.news.hada.io/topic?id=19459, "Dense y Grouped GEMM": the experts' rows are
+ * concatenated along M, each expert's segment aligned to the M block size).
+ * A [M_total][K], sa [K/128][ld_sa], B [num_groups][N][K], sb [num_groups][ceil(N/128)][K/128],
+ * D [M_total][N], m_indices int32 [M_total] on the device: the expert of each row,
+ * or -1 for a padding row.  Padding rows of D are written as +0.
+ * M_total % 128 == 0 (dg_get_mk_alignment_for_contiguous_layout()); every 128-row
+ * block holds rows of one expert, optionally followed by padding rows; a block
+ * whose first row is -1 is all padding. */
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(const void* A, const float* sa, int ld_sa,
+                                                       const void* B, const float* sb, void* D,
+                                                       const int32_t* m_indices, int M_total,
+                                                       int N, int K, int num_groups,
+                                                       void* stream);
+
+/* M-grouped GEMM, masked layout (DeepGEMM "m_grouped_gemm_fp8_fp8_bf16_nt_masked";
+ * es.news.hada.io/topic?id=19459, "Dense y Grouped GEMM": for decoding under CUDA
+ * graphs, where the host does not know how many tokens each expert got).
+ * A [G][max_m][K], sa [G][K/128][ld_sa], B [G][N][K], sb [G][ceil(N/128)][K/128],
+ * D [G][max_m][N], masked_m int32 [G] on the device: rows m < masked_m[g] of group g
+ * are computed; the other rows of D are not written.  The host never reads
+ * masked_m.  expected_m is a hint for the tile-size choice only; results never
+ * depend on it.  1 <= num_groups <= 1024. */
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* sa, int ld_sa,
+                                                   const void* B, const float* sb, void* D,
+                                                   const int32_t* masked_m, int num_groups,
+                                                   int max_m, int N, int K, int expected_m,
+                                                   void* stream);
+
+/* Maximum number of SMs the kernels may use (DeepGEMM set_num_sms / get_num_sms,
+ * es.news.hada.io/topic?id=19459, "Utilidades y variables de entorno").
+ * dg_set_num_sms(0) restores "all SMs of the device"; a value above the device's
+ * SM count is rejected with DG_ERR_INVALID_ARG when a device is present.
+ * dg_get_num_sms() returns the limit in force (the device's SM count by default,
+ * 0 when no device is present and no limit was set). */
+int dg_get_num_sms(void);
+dg_status dg_set_num_sms(int num_sms);
+
+/* Smallest count >= mn whose size in bytes (count * elem_bytes) is a multiple of
+ * 16: the TMA-aligned leading dimension of the transposed scales (DeepGEMM
+ * get_tma_aligned_size, same section).  Returns -1 for mn < 0 or elem_bytes <= 0. */
+int dg_get_tma_aligned_size(int mn, int elem_bytes);
+
+/* Row alignment of each expert's segment in the contiguous layout: the M block
+ * size, 128 (DeepGEMM get_mk_alignment_for_contiguous_layout, same section). */
+int dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* Human-readable detail of the last error returned on this thread ("" if none). */
+const char* dg_last_error_string(void);
+
+/* Waits for `stream`, then returns and clears the device status word of the
+ * current device: DG_OK, or the first device-side error recorded since the last
+ * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE). */
+dg_status dg_get_device_status(void* stream);
+
+/* Tile configuration the library would choose (heuristic, host only; no device
+ * needed).  kind: 0 dense, 1 contiguous, 2 masked.  m is M (dense), M_total
+ * (contiguous) or expected_m (masked).  num_sms is the SM count to plan for. */
+typedef struct dg_config {
+  int block_m;      /* 128 */
+  int block_n;      /* output tile width */
+  int split_k;      /* CTAs per cluster sharing one tile's K groups (dense only) */
+  int stages;       /* depth of the shared-memory ring */
+  int num_tiles;    /* output tiles (masked: from expected_m) */
+  int grid;         /* CTAs launched */
+  int smem_bytes;   /* dynamic shared memory per CTA */
+} dg_config;
+dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
+                         dg_config* out);
+
+/* Number of BLOCK_M x BLOCK_N output tiles of an M x N output (the unit of the
+ * persistent scheduler; deepep.org/zh/deepgemm, "核心优化技术", unaligned block
+ * sizes). Returns -1 for non-positive block sizes. */
+long long dg_num_output_tiles(int m, int n, int block_m, int block_n);
+
+/* Upper bound, in nanoseconds, of every internal wait of the kernels; past it a
+ * kernel records DG_ERR_TIMEOUT and finishes without its result.  0 restores the
+ * default (2 s). */
+dg_status dg_set_wait_timeout_ns(unsigned long long ns);
+
+/* Test hook for the failure path: when nonzero, the next launches run with the
+ * TMA producer switched off, so that their waits run out (DG_ERR_TIMEOUT).  Use
+ * only together with a short dg_set_wait_timeout_ns(). */
+dg_status dg_debug_set_skip_producer(int on);
+
+/* Test and benchmark hook: force the tile width (block_n) and the K split
+ * (split_k, 1..8) of the following launches; 0 leaves that choice to the
+ * heuristic.  A forced configuration the shape cannot use makes the GEMM calls
+ * return DG_ERR_UNSUPPORTED_SHAPE.  The environment variable
+ * DG_FORCE_CONFIG="block_n,split_k" sets the same at start-up. */
+dg_status dg_debug_force_config(int block_n, int split_k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

@@ -1,0 +1,180 @@
+"""Python binding of the GB300 FP8 fine-grained-scaled GEMM library (libdg.so).
+
+Argument marshalling only: every step of the GEMM runs in the library's CUDA
+kernels.  The functions carry the C ABI's names (include/dg.h) without the
+`dg_` prefix and accept either raw device addresses (int) or objects with a
+`data_ptr()` method (torch tensors) for the tensor arguments, and a CUDA stream
+handle (int), a torch stream, or None (torch's current stream when torch is
+loaded, else the legacy default stream).
+
+There is no fallback: if the library has not been built, `lib()` raises.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
+    "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "get_num_sms", "set_num_sms",
+    "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
+    "plan_config", "num_output_tiles", "set_wait_timeout_ns", "debug_set_skip_producer",
+    "debug_force_config", "STATUS_NAMES", "EXPORTED_SYMBOLS",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdg.so")
+
+STATUS_NAMES = {
+    0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED_SHAPE", 3: "DG_ERR_MISALIGNED",
+    4: "DG_ERR_NO_DEVICE", 5: "DG_ERR_ARCH", 6: "DG_ERR_CUDA", 7: "DG_ERR_TIMEOUT",
+    8: "DG_ERR_MASK_RANGE", 9: "DG_ERR_EXPERT_RANGE",
+}
+
+#: Every function include/dg.h declares.
+EXPORTED_SYMBOLS = [
+    "dg_gemm_fp8_fp8_bf16_nt", "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
+    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_get_num_sms", "dg_set_num_sms",
+    "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
+    "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_num_output_tiles",
+    "dg_set_wait_timeout_ns", "dg_debug_set_skip_producer", "dg_debug_force_config",
+]
+
+
+class DGError(RuntimeError):
+    def __init__(self, status, detail):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.name}: {detail}")
+
+
+class DGConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("block_m", "block_n", "split_k", "stages", "num_tiles", "grid", "smem_bytes")]
+
+
+_LIB = None
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built (no fallback)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m moe_grouped_gemm_bf16_gb300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.dg_gemm_fp8_fp8_bf16_nt.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]
+        L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+        L.dg_get_num_sms.argtypes = []
+        L.dg_set_num_sms.argtypes = [_i]
+        L.dg_get_tma_aligned_size.argtypes = [_i, _i]
+        L.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
+        L.dg_last_error_string.argtypes = []
+        L.dg_last_error_string.restype = ctypes.c_char_p
+        L.dg_get_device_status.argtypes = [_vp]
+        L.dg_plan_config.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(DGConfig)]
+        L.dg_num_output_tiles.argtypes = [_i, _i, _i, _i]
+        L.dg_num_output_tiles.restype = ctypes.c_longlong
+        L.dg_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        L.dg_debug_set_skip_producer.argtypes = [_i]
+        L.dg_debug_force_config.argtypes = [_i, _i]
+        for f in EXPORTED_SYMBOLS:
+            if f not in ("dg_last_error_string", "dg_num_output_tiles"):
+                getattr(L, f).restype = _i
+        _LIB = L
+    return _LIB
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except Exception:  # pragma: no cover
+            pass
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(status):
+    if status != 0:
+        raise DGError(status, lib().dg_last_error_string().decode())
+
+
+def gemm_fp8_fp8_bf16_nt(A, sa, ld_sa, B, sb, D, M, N, K, stream=None):
+    """D[M,N] = bf16(sum_g (A_g B_g^T) sa sb); see dg_gemm_fp8_fp8_bf16_nt."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_nt(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D),
+                                         M, N, K, _stream(stream)))
+
+
+def m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(A, sa, ld_sa, B, sb, D, m_indices, M_total, N, K,
+                                              num_groups, stream=None):
+    _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(
+        _ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D), _ptr(m_indices), M_total, N, K,
+        num_groups, _stream(stream)))
+
+
+def m_grouped_gemm_fp8_fp8_bf16_nt_masked(A, sa, ld_sa, B, sb, D, masked_m, num_groups, max_m,
+                                          N, K, expected_m, stream=None):
+    _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(
+        _ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D), _ptr(masked_m), num_groups, max_m,
+        N, K, expected_m, _stream(stream)))
+
+
+def get_num_sms():
+    return int(lib().dg_get_num_sms())
+
+
+def set_num_sms(n):
+    _check(lib().dg_set_num_sms(int(n)))
+
+
+def get_tma_aligned_size(mn, elem_bytes):
+    return int(lib().dg_get_tma_aligned_size(int(mn), int(elem_bytes)))
+
+
+def get_mk_alignment_for_contiguous_layout():
+    return int(lib().dg_get_mk_alignment_for_contiguous_layout())
+
+
+def get_device_status(stream=None):
+    """Status code (int) of the device status word, which is then cleared."""
+    return int(lib().dg_get_device_status(_stream(stream)))
+
+
+def plan_config(kind, m, n, k, num_groups=1, num_sms=152):
+    cfg = DGConfig()
+    _check(lib().dg_plan_config(int(kind), int(m), int(n), int(k), int(num_groups), int(num_sms),
+                                ctypes.byref(cfg)))
+    return {f: getattr(cfg, f) for f, _ in DGConfig._fields_}
+
+
+def num_output_tiles(m, n, block_m, block_n):
+    return int(lib().dg_num_output_tiles(int(m), int(n), int(block_m), int(block_n)))
+
+
+def set_wait_timeout_ns(ns):
+    _check(lib().dg_set_wait_timeout_ns(int(ns)))
+
+
+def debug_set_skip_producer(on):
+    _check(lib().dg_debug_set_skip_producer(1 if on else 0))
+
+
+def debug_force_config(block_n=0, split_k=0):
+    _check(lib().dg_debug_force_config(int(block_n), int(split_k)))

@@ -1,0 +1,538 @@
+// Host side of the C ABI (include/dg.h): argument validation, the tile-size
+// heuristic, TMA tensor-map encoding and the launch of the sm_103a kernels.
+//
+// The entry points follow DeepGEMM's interface (deepep.org/zh/deepgemm,
+// "接口设计"; es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
+// layout", "Dense y Grouped GEMM", "Utilidades y variables de entorno").
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dg.h"
+#include "dg_instances.cuh"
+
+// The device status word: kernels record the first device-side error here.
+__device__ unsigned int g_dg_status = 0;
+
+namespace {
+
+using dgk::Instance;
+
+thread_local std::string t_err;
+
+dg_status fail(dg_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+dg_status ok() {
+  t_err.clear();
+  return DG_OK;
+}
+
+std::atomic<int> g_num_sms_limit{0};
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_skip_producer{0};
+std::atomic<int> g_force_bn{-1};     // -1: not read from the environment yet; 0: auto
+std::atomic<int> g_force_split{0};
+
+constexpr int kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class GPUs
+constexpr int kMaxDevices = 64;
+constexpr int kMaxCluster = 8;
+constexpr int kRasterM = 16;
+
+void read_env_once() {
+  int expected = -1;
+  if (!g_force_bn.compare_exchange_strong(expected, 0)) return;
+  // DG_FORCE_CONFIG="block_n,split_k" (tests and benchmarks only)
+  if (const char* s = std::getenv("DG_FORCE_CONFIG")) {
+    int bn = 0, sp = 0;
+    if (std::sscanf(s, "%d,%d", &bn, &sp) >= 1) {
+      g_force_bn.store(bn);
+      g_force_split.store(sp);
+    }
+  }
+}
+
+bool print_configs() {
+  const char* s = std::getenv("DG_PRINT_CONFIGS");
+  return s && s[0] && s[0] != '0';
+}
+
+// ------------------------------------------------------------ instances --
+struct Table {
+  const Instance* p;
+  int n;
+};
+
+Table table_for(int kind) {
+  Table t{nullptr, 0};
+  if (kind == dgk::kDense) t.p = dgk::instances_dense(&t.n);
+  else if (kind == dgk::kContiguous) t.p = dgk::instances_contiguous(&t.n);
+  else t.p = dgk::instances_masked(&t.n);
+  return t;
+}
+
+int smem_for(const Instance& in, int kb, int num_groups) {
+  int s = in.fixed_smem + 3 * kb * 4 + (in.mode == dgk::kMasked ? (2 * num_groups + 1) * 4 : 0);
+  return (s + 15) & ~15;
+}
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ heuristic --
+// A plan: one instance, the K split (cluster size) and the persistent grid.
+struct Plan {
+  int inst = -1;
+  int split = 1;
+  long long tiles = 0;
+  int clusters = 0;
+  int smem = 0;
+};
+
+// cap(S): clusters of S CTAs that can be resident at once.
+template <typename Cap>
+Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sms, Cap cap,
+            int force_bn, int force_split) {
+  const Table tab = table_for(kind);
+  const int kb = k / 128;
+  Plan best;
+  double best_cost = 1e300;
+  for (int i = 0; i < tab.n; ++i) {
+    const Instance& in = tab.p[i];
+    if (force_bn > 0 && in.block_n != force_bn) continue;
+    const int smem = smem_for(in, kb, num_groups);
+    if (smem > kMaxSmem) continue;
+    const int s_lo = in.split ? 2 : 1;
+    const int s_hi = in.split ? std::min(kMaxCluster, kb) : 1;
+    for (int S = s_lo; S <= s_hi; ++S) {
+      if (force_split > 0 && S != force_split) continue;
+      if (force_split == 0 && force_bn > 0 && in.split) {
+        // a forced block_n without a forced split keeps the unsplit instance
+        continue;
+      }
+      long long mblk;
+      if (kind == dgk::kMasked) mblk = (long long)num_groups * cdiv(m_rows, 128);
+      else mblk = cdiv(m_rows, 128);
+      const long long tiles = mblk * cdiv(n, in.block_n);
+      const long long c = std::max(1, cap(i, in, S, smem));
+      const long long waves = cdiv(tiles, c);
+      const long long kper = cdiv(kb, S);
+      // bytes each CTA streams per K group, in units of 128 B rows: A (128) + B (BN)
+      double cost = (double)waves * ((double)kper * (128 + in.block_n) +
+                                     (S > 1 ? 4.0 * (128 + in.block_n) : 0.0) + 8.0 * 128);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.inst = i;
+        best.split = S;
+        best.tiles = tiles;
+        best.clusters = (int)std::min<long long>(tiles, c);
+        best.smem = smem;
+      }
+    }
+  }
+  (void)num_sms;
+  return best;
+}
+
+}  // namespace
+
+namespace {
+
+// ------------------------------------------------------- device state ----
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  unsigned int* status = nullptr;
+  // resident clusters per (form, instance, split)
+  int max_clusters[3][8][kMaxCluster + 1] = {};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+dg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Set-up of the current device, once: architecture check, the status word's
+// address, the tensor-map encoder, and the shared-memory limit of every
+// instance.
+dg_status device_state(DeviceState** out, int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DG_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+  }
+  if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_NO_DEVICE, "device index %d", dev);
+  DeviceState& st = g_dev[dev];
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (st.ready) {
+    *out = &st;
+    return DG_OK;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(DG_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                minor);
+  void* sp = nullptr;
+  if ((e = cudaGetSymbolAddress(&sp, g_dg_status)) != cudaSuccess)
+    return cuda_fail(e, "cudaGetSymbolAddress(status)");
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  for (int kind = 0; kind < 3; ++kind) {
+    const Table tab = table_for(kind);
+    for (int i = 0; i < tab.n; ++i)
+      if ((e = tab.p[i].set_smem(kMaxSmem)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  }
+  st.sms = sms;
+  st.status = static_cast<unsigned int*>(sp);
+  st.ready = true;
+  *out = &st;
+  return DG_OK;
+}
+
+int clusters_resident(DeviceState& st, int kind, int inst, const Instance& in, int S, int smem,
+                      int num_sms) {
+  if (S <= 1) return num_sms;
+  int& slot = st.max_clusters[kind][inst][S];
+  if (slot == 0) {
+    int n = 0;
+    if (in.max_clusters(S, kMaxSmem, &n) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = -1;
+    }
+    slot = n;
+  }
+  (void)smem;
+  if (slot < 0) return 0;
+  // a limit on SMs caps the clusters too
+  return std::min(slot, std::max(1, num_sms / S));
+}
+
+int sms_in_use(const DeviceState& st) {
+  const int lim = g_num_sms_limit.load();
+  return (lim > 0 && lim < st.sms) ? lim : st.sms;
+}
+
+// ------------------------------------------------------------ tensor maps --
+dg_status encode(CUtensorMap* m, CUtensorMapDataType dt, void* ptr, const uint64_t dims[3],
+                 const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw,
+                 CUtensorMapL2promotion l2, const char* name) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, ptr, reinterpret_cast<const cuuint64_t*>(dims),
+                        reinterpret_cast<const cuuint64_t*>(strides),
+                        reinterpret_cast<const cuuint32_t*>(box), estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+  return DG_OK;
+}
+
+// A [z][rows][K] e4m3, B [g][N][K] e4m3, sa [z][kb][ld_sa] fp32, D [z][rows][N] bf16.
+dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, const void* B,
+                    void* D, int rows, int zA, int N, int K, int gB, int block_n) {
+  const int kb = K / 128;
+  {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)zA};
+    const uint64_t str[2] = {(uint64_t)K, (uint64_t)rows * K};
+    const uint32_t box[3] = {128, 128, 1};
+    dg_status s = encode(&mp->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(A), dims, str,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
+    if (s != DG_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)gB};
+    const uint64_t str[2] = {(uint64_t)K, (uint64_t)N * K};
+    const uint32_t box[3] = {128, (uint32_t)block_n, 1};
+    dg_status s = encode(&mp->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(B), dims, str,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
+    if (s != DG_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)ld_sa, (uint64_t)kb, (uint64_t)zA};
+    const uint64_t str[2] = {(uint64_t)ld_sa * 4, (uint64_t)kb * ld_sa * 4};
+    const uint32_t box[3] = {128, 1, 1};
+    dg_status s = encode(&mp->sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(sa), dims,
+                         str, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         "sa");
+    if (s != DG_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)rows, (uint64_t)zA};
+    const uint64_t str[2] = {(uint64_t)N * 2, (uint64_t)rows * N * 2};
+    const uint32_t box[3] = {32, 128, 1};
+    dg_status s = encode(&mp->d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, dims, str, box,
+                         CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
+    if (s != DG_OK) return s;
+  }
+  return DG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+namespace {
+
+const char* kind_name(int kind) {
+  return kind == dgk::kDense ? "dense" : kind == dgk::kContiguous ? "contiguous" : "masked";
+}
+
+// Shared path of the three GEMM entry points.  rows = M (dense), M_total
+// (contiguous) or max_m (masked); idx = m_indices or masked_m.
+dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B, const float* sb,
+              void* D, const int32_t* idx, int rows, int N, int K, int G, int expected_m,
+              void* stream) {
+  read_env_once();
+  // -------- validation (host only; nothing is launched on an error) ------
+  if (rows < 0 || N < 0 || K < 0)
+    return fail(DG_ERR_INVALID_ARG, "negative size (rows=%d, N=%d, K=%d)", rows, N, K);
+  if (kind != dgk::kDense && (G < 1 || (kind == dgk::kMasked && G > dgk::MAX_GROUPS_MASKED)))
+    return fail(DG_ERR_INVALID_ARG, "num_groups=%d outside [1, %d]", G,
+                kind == dgk::kMasked ? dgk::MAX_GROUPS_MASKED : 0x7fffffff);
+  if (K % 128 != 0 || K < 128 || K > 128 * dgk::MAX_KB)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "K=%d: need a multiple of 128 in [128, %d]", K,
+                128 * dgk::MAX_KB);
+  if (N % 16 != 0 || N < 16)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "N=%d: need a multiple of 16, at least 16", N);
+  if (kind == dgk::kContiguous && rows % 128 != 0)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "M_total=%d is not a multiple of 128", rows);
+  if (!A || !sa || !B || !sb || !D)
+    return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
+  if (kind != dgk::kDense && !idx)
+    return fail(DG_ERR_INVALID_ARG, "null %s", kind == dgk::kMasked ? "masked_m" : "m_indices");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sa) ||
+      (reinterpret_cast<uintptr_t>(sb) & 3u) || (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
+    return fail(DG_ERR_MISALIGNED, "A, B, D and sa need 16-byte alignment, sb and indices 4");
+  if (ld_sa < rows || ld_sa % 4 != 0 || ld_sa < 1)
+    return fail(ld_sa % 4 != 0 ? DG_ERR_MISALIGNED : DG_ERR_INVALID_ARG,
+                "ld_sa=%d: need >= %d and a multiple of 4", ld_sa, rows);
+  if ((long long)rows * (long long)G >= (1ll << 31) || (long long)N * K >= (1ll << 40))
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "tensor too large");
+  if (rows == 0) return ok();  // nothing to compute
+
+  // -------- device, plan, tensor maps, launch ------------------------------
+  DeviceState* st = nullptr;
+  int dev = 0;
+  dg_status s = device_state(&st, &dev);
+  if (s != DG_OK) return s;
+  const int num_sms = sms_in_use(*st);
+  auto cap = [&](int i, const Instance& in, int S, int smem) {
+    return S <= 1 ? num_sms : clusters_resident(*st, kind, i, in, S, smem, num_sms);
+  };
+  const int m_plan = kind == dgk::kMasked ? std::max(1, std::min(expected_m, rows)) : rows;
+  const Plan pl = choose(kind, m_plan, N, K, G, num_sms, cap, g_force_bn.load(),
+                         g_force_split.load());
+  if (pl.inst < 0)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "no kernel configuration for this shape%s",
+                g_force_bn.load() > 0 ? " (DG_FORCE_CONFIG)" : "");
+  const Instance& in = table_for(kind).p[pl.inst];
+  int clusters = pl.clusters;
+  if (kind == dgk::kMasked) {
+    const long long ub = (long long)G * cdiv(rows, 128) * cdiv(N, in.block_n);
+    clusters = (int)std::min<long long>(ub, num_sms);
+  }
+  const int grid = std::max(1, clusters) * pl.split;
+
+  dgk::Maps maps;
+  s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
+                kind == dgk::kDense ? 1 : G, in.block_n);
+  if (s != DG_OK) return s;
+
+  dgk::Params p{};
+  p.M = rows;
+  p.N = N;
+  p.K = K;
+  p.kb = K / 128;
+  p.nb = (N + 127) / 128;
+  p.num_groups = kind == dgk::kDense ? 1 : G;
+  p.num_m_blocks = (int)cdiv(rows, 128);
+  p.num_n_blocks = (int)cdiv(N, in.block_n);
+  p.raster_m = kRasterM;
+  p.split_k = pl.split;
+  p.sb = sb;
+  p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
+  p.masked_m = kind == dgk::kMasked ? idx : nullptr;
+  p.D = static_cast<uint16_t*>(D);
+  p.status = st->status;
+  p.timeout_ns = g_timeout_ns.load();
+  p.debug_flags = g_skip_producer.load() ? dgk::DBG_SKIP_PRODUCER : 0u;
+
+  const cudaError_t e = in.launch(maps, p, grid, pl.split, pl.smem,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "kernel launch");
+  }
+  if (print_configs())
+    std::fprintf(stderr,
+                 "[dg] %s M=%d N=%d K=%d G=%d: block_n=%d split_k=%d stages=%d tiles=%lld "
+                 "grid=%d smem=%d\n",
+                 kind_name(kind), rows, N, K, G, in.block_n, pl.split, in.stages,
+                 (long long)pl.tiles, grid, pl.smem);
+  return ok();
+}
+
+}  // namespace
+
+// ====================================================================== ABI ==
+extern "C" {
+
+dg_status dg_gemm_fp8_fp8_bf16_nt(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, void* D, int M, int N, int K, void* stream) {
+  return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream);
+}
+
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(const void* A, const float* sa, int ld_sa,
+                                                       const void* B, const float* sb, void* D,
+                                                       const int32_t* m_indices, int M_total,
+                                                       int N, int K, int num_groups,
+                                                       void* stream) {
+  return run(dgk::kContiguous, A, sa, ld_sa, B, sb, D, m_indices, M_total, N, K, num_groups,
+             M_total, stream);
+}
+
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* sa, int ld_sa,
+                                                   const void* B, const float* sb, void* D,
+                                                   const int32_t* masked_m, int num_groups,
+                                                   int max_m, int N, int K, int expected_m,
+                                                   void* stream) {
+  return run(dgk::kMasked, A, sa, ld_sa, B, sb, D, masked_m, max_m, N, K, num_groups, expected_m,
+             stream);
+}
+
+int dg_get_num_sms(void) {
+  const int lim = g_num_sms_limit.load();
+  if (lim > 0) return lim;
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return sms;
+}
+
+dg_status dg_set_num_sms(int num_sms) {
+  if (num_sms < 0) return fail(DG_ERR_INVALID_ARG, "num_sms=%d < 0", num_sms);
+  int dev = -1, sms = 0;
+  if (num_sms > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      num_sms > sms)
+    return fail(DG_ERR_INVALID_ARG, "num_sms=%d exceeds the device's %d SMs", num_sms, sms);
+  cudaGetLastError();
+  g_num_sms_limit.store(num_sms);
+  return ok();
+}
+
+int dg_get_tma_aligned_size(int mn, int elem_bytes) {
+  if (mn < 0 || elem_bytes <= 0) return -1;
+  // smallest multiple of (16 / gcd(16, elem_bytes)) elements not below mn
+  int g = 16, e = elem_bytes;
+  while (e) { int t = g % e; g = e; e = t; }
+  const int unit = 16 / g;
+  return (mn + unit - 1) / unit * unit;
+}
+
+int dg_get_mk_alignment_for_contiguous_layout(void) { return dgk::BLOCK_M; }
+
+const char* dg_last_error_string(void) { return t_err.c_str(); }
+
+dg_status dg_get_device_status(void* stream) {
+  DeviceState* st = nullptr;
+  int dev = 0;
+  dg_status s = device_state(&st, &dev);
+  if (s != DG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0, zero = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_dg_status, sizeof(v))) != cudaSuccess)
+    return cuda_fail(e, "read status");
+  if ((e = cudaMemcpyToSymbol(g_dg_status, &zero, sizeof(zero))) != cudaSuccess)
+    return cuda_fail(e, "clear status");
+  switch (v) {
+    case dgk::ST_OK: return ok();
+    case dgk::ST_TIMEOUT: return fail(DG_ERR_TIMEOUT, "a kernel wait timed out");
+    case dgk::ST_MASK_RANGE: return fail(DG_ERR_MASK_RANGE, "masked_m outside [0, max_m]");
+    case dgk::ST_EXPERT_RANGE:
+      return fail(DG_ERR_EXPERT_RANGE, "m_indices out of range or a block mixes experts");
+    default: return fail(DG_ERR_CUDA, "unknown device status %u", v);
+  }
+}
+
+dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
+                         dg_config* out) {
+  read_env_once();
+  if (!out || kind < 0 || kind > 2 || m < 1 || n < 16 || n % 16 || k < 128 || k % 128 ||
+      k > 128 * dgk::MAX_KB || num_sms < 1 || (kind != dgk::kDense && num_groups < 1))
+    return fail(DG_ERR_INVALID_ARG, "dg_plan_config: bad arguments");
+  const int G = kind == dgk::kDense ? 1 : num_groups;
+  auto cap = [&](int, const Instance&, int S, int) { return S <= 1 ? num_sms : num_sms / S; };
+  const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load());
+  if (pl.inst < 0) return fail(DG_ERR_UNSUPPORTED_SHAPE, "no configuration");
+  const Instance& in = table_for(kind).p[pl.inst];
+  out->block_m = dgk::BLOCK_M;
+  out->block_n = in.block_n;
+  out->split_k = pl.split;
+  out->stages = in.stages;
+  out->num_tiles = (int)pl.tiles;
+  out->grid = std::max(1, pl.clusters) * pl.split;
+  out->smem_bytes = pl.smem;
+  return ok();
+}
+
+long long dg_num_output_tiles(int m, int n, int block_m, int block_n) {
+  if (block_m <= 0 || block_n <= 0 || m < 0 || n < 0) return -1;
+  return cdiv(m, block_m) * cdiv(n, block_n);
+}
+
+dg_status dg_set_wait_timeout_ns(unsigned long long ns) {
+  g_timeout_ns.store(ns ? ns : 2000000000ull);
+  return ok();
+}
+
+dg_status dg_debug_set_skip_producer(int on) {
+  g_skip_producer.store(on ? 1 : 0);
+  return ok();
+}
+
+dg_status dg_debug_force_config(int block_n, int split_k) {
+  read_env_once();
+  if (block_n < 0 || split_k < 0 || split_k > kMaxCluster)
+    return fail(DG_ERR_INVALID_ARG, "block_n=%d split_k=%d", block_n, split_k);
+  g_force_bn.store(block_n);
+  g_force_split.store(split_k);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Ahead-of-time kernel instances and their launch helpers.  Each instance is a
+// fixed (BLOCK_N, stages, K split, form) combination of the kernel template;
+// the host launcher picks one per call.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dg_params.h"
+
+namespace dgk {
+
+struct Maps {
+  CUtensorMap a, b, sa, d;
+};
+
+struct Instance {
+  int block_n;
+  int stages;
+  int split;  // 1: may run as a cluster with the K groups split across its CTAs
+  int mode;
+  int fixed_smem;  // shared memory that does not depend on the shape (bytes)
+  cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
+                        cudaStream_t s);
+  cudaError_t (*set_smem)(int smem);
+  cudaError_t (*max_clusters)(int cluster, int smem, int* out);
+};
+
+// Per-form instance tables (defined in dg_inst_*.cu).
+const Instance* instances_dense(int* count);
+const Instance* instances_contiguous(int* count);
+const Instance* instances_masked(int* count);
+
+}  // namespace dgk
+
+#ifdef DGK_DEFINE_INSTANCES
+#include "dg_kernel.cuh"
+
+namespace dgk {
+
+template <int BN, int STAGES, bool SPLIT, int MODE>
+struct InstanceOf {
+  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE>;
+
+  static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
+                            cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = SPLIT ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.sa, m.d, p);
+  }
+
+  static cudaError_t set_smem(int smem) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  }
+
+  static cudaError_t max_clusters(int cluster, int smem, int* out) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
+  }
+
+  static Instance make() {
+    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, SmemLayout<BN, STAGES, SPLIT>::DYN_OFF + 1024,
+                    &launch, &set_smem, &max_clusters};
+  }
+};
+
+}  // namespace dgk
+#endif

@@ -1,0 +1,551 @@
+// The FP8 fine-grained-scaled GEMM kernel for sm_103a (dense, contiguous and
+// masked M-grouped forms), written for GB300's tensor memory and TMA.
+//
+// What it computes (DeepGEMM, es.news.hada.io/topic?id=19459, "Interfaz GEMM
+// y restricciones de layout" and "Dense y Grouped GEMM"):
+//   D[m,n] = bf16( sum_g (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
+// with A e4m3 [M,K], B e4m3 [N,K] (NT), one fp32 scale per row per 128-wide K
+// group for A (stored K-group-major) and one per 128x128 block for B.
+//
+// Structure (one persistent CTA per SM, or one cluster of split_k CTAs):
+//   warp 0      TMA producer: A tile [128 x 128], B tile [BN x 128] into an
+//               S-stage ring; the 128 activation scales of the K group into a
+//               separate ring (they are read later, by the promotion warps).
+//   warp 1      allocates tensor memory; one thread issues 4 tcgen05.mma
+//               (K = 32 each) per K group into one of two TMEM accumulators,
+//               then commits: the stage goes back to the producer, the
+//               accumulator goes to the promotion warps.
+//   warps 4..11 promotion (two warpgroups): read the group's fp32 partial from TMEM, scale it by
+//               sa[m,g] * sb[n/128,g] and add it into fp32 registers while the
+//               tensor cores already compute the next group (the two-level
+//               accumulation of the pages: DeepSeek's overview
+//               deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
+//               Then the bf16 epilogue: a swizzled staging tile stored by TMA,
+//               or, when the K groups are split over a cluster, a fixed-order
+//               reduction of the partials through distributed shared memory.
+//
+// Every mbarrier wait is bounded: when one gives up it records a timeout in
+// the device status word and sets a CTA-wide abort flag, after which every
+// wait returns at once and no further TMA or MMA is issued, so the kernel runs
+// to its normal end (all hardware barriers matched, TMEM freed) without
+// hanging.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "dg_params.h"
+#include "ptx.cuh"
+
+namespace dgk {
+
+template <int BN, int STAGES, bool SPLIT>
+struct SmemLayout {
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K;  // 16 KB e4m3
+  static constexpr int B_BYTES = BN * BLOCK_K;
+  static constexpr int SA_BYTES = BLOCK_M * 4;       // 512 B fp32
+  static constexpr int A_OFF = 0;
+  static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+  static constexpr int SA_OFF = B_OFF + STAGES * B_BYTES;
+  static constexpr int OUT_OFF = SA_OFF + SA_SLOTS * SA_BYTES;
+  // bf16 staging for the TMA store, or the fp32 partial for the split reduction
+  static constexpr int OUT_BYTES = SPLIT ? BLOCK_M * BN * 4 : BLOCK_M * BN * 2;
+  static constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
+  // barrier indexes
+  static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
+                       SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
+                       T_EMPTY = T_FULL + 2, RED_FULL = T_EMPTY + 2, RED_EMPTY = RED_FULL + 1,
+                       MMA_DONE = RED_EMPTY + 1, NUM_BARS = MMA_DONE + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int DYN_OFF = MISC_OFF + 16;            // sb tile, then masked tables
+  static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+};
+
+// Dynamic shared memory a launch needs (host side too).
+template <int BN, int STAGES, bool SPLIT>
+__host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
+  return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT>::DYN_OFF + 3 * kb * 4 +
+         (mode == kMasked ? (2 * num_groups + 1) * 4 : 0);
+}
+
+struct Tile {
+  int m0;     // first row of the tile, within its group
+  int n0;     // first column
+  int z;      // group coordinate of A / sa / D (masked form), else 0
+  int e;      // expert / group of B and sb
+  int rows;   // rows that hold valid output
+  int skip;   // 1: contiguous padding block (no MMA, +0 output); 2: bad expert id
+};
+
+__device__ __forceinline__ void raise_status(const Params& p, unsigned int code) {
+  atomicCAS(p.status, 0u, code);
+}
+
+// Tile t of the persistent schedule.  Tiles are numbered in raster bands of
+// `raster_m` M blocks: within a band, consecutive tiles walk down the band's M
+// blocks and then across N, so the tiles running at the same time share A
+// rows and B columns in L2 (block scheduler with rasterisation, DeepGEMM
+// overview deepep.org/zh/deepgemm, "统一优化的块调度器").
+template <int BN, int MODE>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_blocks,
+                                            const int* prefix, const int* mcnt) {
+  const int nN = p.num_n_blocks;
+  const int band_tiles = p.raster_m * nN;
+  const int band = t / band_tiles;
+  const int r = t - band * band_tiles;
+  const int bm0 = band * p.raster_m;
+  const int bh = min(p.raster_m, num_m_blocks - bm0);
+  const int mb = bm0 + r % bh;
+  Tile T;
+  T.n0 = (r / bh) * BN;
+  T.skip = 0;
+  if (MODE == kDense) {
+    T.m0 = mb * BLOCK_M;
+    T.z = 0;
+    T.e = 0;
+    T.rows = min(BLOCK_M, p.M - T.m0);
+  } else if (MODE == kContiguous) {
+    T.m0 = mb * BLOCK_M;
+    T.z = 0;
+    const int e = __ldg(p.m_indices + T.m0);
+    T.e = e;
+    T.rows = BLOCK_M;
+    if (e < 0) {
+      T.skip = 1;
+      T.e = 0;
+    } else if (e >= p.num_groups) {
+      T.skip = 2;
+      T.e = 0;
+    }
+  } else {
+    // flat M block -> group: largest g with prefix[g] <= mb
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= mb) lo = mid; else hi = mid - 1;
+    }
+    T.z = lo;
+    T.e = lo;
+    T.m0 = (mb - prefix[lo]) * BLOCK_M;
+    T.rows = min(BLOCK_M, mcnt[lo] - T.m0);
+  }
+  return T;
+}
+
+// Bounded mbarrier wait.  Returns false (without waiting) once the CTA has
+// aborted, or after `timeout_ns`, in which case it records the timeout and
+// aborts the CTA.
+template <bool ACQ_CLUSTER = false>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         const Params& p) {
+  auto try_once = [&]() {
+    return ACQ_CLUSTER ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
+  if (*abort_flag) return false;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (!try_once()) {
+    if ((++it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        raise_status(p, ST_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Wait used while draining at the end: ignores the abort flag, gives up only
+// on the time limit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Params& p) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      raise_status(p, ST_TIMEOUT);
+      return;
+    }
+  }
+}
+
+}  // namespace dgk
+
+namespace dgk {
+
+template <int BN, int STAGES, bool SPLIT, int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
+                const Params p) {
+  static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
+  using L = SmemLayout<BN, STAGES, SPLIT>;
+  constexpr int HALF = BN / 2;                 // columns per promotion warpgroup
+  constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup
+  constexpr int LDS_PER_WAIT = (HALF >= 128) ? 1 : 2;
+  constexpr uint32_t IDESC = idesc_e4m3_f32(BLOCK_M, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  // swizzled tiles need 1024-byte aligned shared-memory addresses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8 * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile uint32_t* abort_flag = misc + 1;
+  float* sb_s = reinterpret_cast<float*>(smem + L::DYN_OFF);
+  int* prefix = reinterpret_cast<int*>(sb_s + 3 * p.kb);
+  int* mcnt = prefix + p.num_groups + 1;
+  const float* sa_ring = reinterpret_cast<const float*>(smem + L::SA_OFF);
+
+  const uint32_t crank = SPLIT ? cluster_ctarank() : 0;
+  const int S = SPLIT ? p.split_k : 1;
+  const int cluster_id = blockIdx.x / S;
+  const int num_clusters = gridDim.x / S;
+  const int kbeg = static_cast<int>(static_cast<long long>(crank) * p.kb / S);
+  const int kend = static_cast<int>(static_cast<long long>(crank + 1) * p.kb / S);
+  const int kcnt = kend - kbeg;
+
+  // ------------------------------------------------------------- set-up --
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(L::FULL + s), 1);
+      mbar_init(bar(L::EMPTY + s), 1);
+    }
+    for (int j = 0; j < SA_SLOTS; ++j) {
+      mbar_init(bar(L::SA_FULL + j), 1);
+      mbar_init(bar(L::SA_EMPTY + j), NUM_PROMO_WARPS);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::T_FULL + b), 1);
+      mbar_init(bar(L::T_EMPTY + b), NUM_PROMO_WARPS);
+    }
+    mbar_init(bar(L::RED_FULL), S);
+    mbar_init(bar(L::RED_EMPTY), S);
+    mbar_init(bar(L::MMA_DONE), 1);
+    misc[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (MODE == kMasked && warp == 2) {  // (warp 2 is otherwise idle)
+    // valid rows per group (clamped to [0, max_m]) and the prefix sum of M blocks
+    int carry = 0;
+    for (int base = 0; base < p.num_groups; base += 32) {
+      const int g = base + lane;
+      int c = 0;
+      if (g < p.num_groups) {
+        const int v = __ldg(p.masked_m + g);
+        const int vc = min(max(v, 0), p.M);
+        if (vc != v && blockIdx.x == 0) raise_status(p, ST_MASK_RANGE);
+        mcnt[g] = vc;
+        c = (vc + BLOCK_M - 1) / BLOCK_M;
+      }
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (g < p.num_groups) prefix[g + 1] = carry + x;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (SPLIT) cluster_sync();
+  const uint32_t tmem_base = misc[0];
+  const int num_m_blocks = (MODE == kMasked) ? prefix[p.num_groups] : p.num_m_blocks;
+  const int num_tiles = num_m_blocks * p.num_n_blocks;
+
+  // A 256-column tile needs 128 accumulator registers per promotion thread:
+  // move registers from warpgroup 0 (TMA, MMA, two idle warps) to the two
+  // promotion warpgroups.  Per SM sub-partition: 40 + 2 * 232 = 3 * 168.
+  constexpr bool REALLOC = (HALF >= 128);
+
+  if (warp < 4) {
+  if constexpr (REALLOC) regs_dec<40>();
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0 && !(p.debug_flags & DBG_SKIP_PRODUCER)) {
+      // per slot: was a load issued, and with which phase parity
+      uint32_t issued_mask = 0, issued_par = 0, sa_issued_mask = 0, sa_issued_par = 0;
+      int s = 0, j = 0;
+      uint32_t ph = 0, jph = 0;
+      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+        if (T.skip) continue;
+        for (int g = kbeg; g < kend; ++g) {
+          if (wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p)) {
+            mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + L::B_BYTES);
+            tma_load_3d(sbase + L::A_OFF + s * L::A_BYTES, &tmA, bar(L::FULL + s), g * BLOCK_K,
+                        T.m0, T.z);
+            tma_load_3d(sbase + L::B_OFF + s * L::B_BYTES, &tmB, bar(L::FULL + s), g * BLOCK_K,
+                        T.n0, T.e);
+            issued_mask |= 1u << s;
+            issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          }
+          if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
+            mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
+            tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0, g,
+                        T.z);
+            sa_issued_mask |= 1u << j;
+            sa_issued_par = (sa_issued_par & ~(1u << j)) | (jph << j);
+          }
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+          if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+        }
+      }
+      // Drain: after an abort the latest load into a slot may still be in
+      // flight; wait for it before the CTA can exit.  (After a normal run every
+      // load has been consumed already and these waits return at once.)
+      for (int q = 0; q < STAGES; ++q)
+        if ((issued_mask >> q) & 1u) drain_wait(bar(L::FULL + q), (issued_par >> q) & 1u, p);
+      for (int q = 0; q < SA_SLOTS; ++q)
+        if ((sa_issued_mask >> q) & 1u) drain_wait(bar(L::SA_FULL + q), (sa_issued_par >> q) & 1u, p);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      int s = 0, b = 0;
+      uint32_t ph = 0, bph = 0;
+      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+        if (T.skip) continue;
+        for (int g = kbeg; g < kend; ++g) {
+          const bool ok_t = wait_bar(bar(L::T_EMPTY + b), bph ^ 1, abort_flag, p);
+          tc_fence_after();
+          const bool ok_f = wait_bar(bar(L::FULL + s), ph, abort_flag, p);
+          tc_fence_after();
+          if (ok_t && ok_f) {
+            const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
+            const uint64_t ad = smem_desc_sw128_kmajor(sbase + L::A_OFF + s * L::A_BYTES);
+            const uint64_t bd = smem_desc_sw128_kmajor(sbase + L::B_OFF + s * L::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BLOCK_K / 32; ++kk)
+              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+            mma_commit(bar(L::EMPTY + s));
+            mma_commit(bar(L::T_FULL + b));
+          }
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+          if (++b == 2) { b = 0; bph ^= 1; }
+        }
+      }
+      // nothing issued may still run when the TMEM is freed
+      mma_commit(bar(L::MMA_DONE));
+      drain_wait(bar(L::MMA_DONE), 0, p);
+    }
+    __syncwarp();
+  }
+  } else {
+    if constexpr (REALLOC) regs_inc<232>();
+    // -------------------------------------------------- promotion warps ---
+    const int pw = warp - 4;            // 0..7
+    const int q = warp & 3;             // TMEM lane quadrant this warp may access
+    const int h = pw >> 2;              // which half of the tile's columns
+    const int row = q * 32 + lane;      // the tile row this thread owns
+    const int pt = threadIdx.x - 128;   // 0..255 among the promotion threads
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t out_s = sbase + L::OUT_OFF;
+    int b = 0, j = 0;
+    uint32_t bph = 0, jph = 0;
+    uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
+    float acc[HALF];
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++k_iter) {
+      const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+      // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
+      named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+      if (!T.skip) {
+        const int blk0 = T.n0 >> 7;
+        for (int i = pt; i < 3 * kcnt; i += 32 * NUM_PROMO_WARPS) {
+          const int jb = i / kcnt, gg = i - jb * kcnt;
+          const int nbk = min(blk0 + jb, p.nb - 1);
+          sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + kbeg + gg);
+        }
+      }
+      named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
+      if (!T.skip) {
+        const int nmod = T.n0 & 127;
+        for (int g = kbeg; g < kend; ++g) {
+          wait_bar(bar(L::T_FULL + b), bph, abort_flag, p);
+          wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
+          __syncwarp();
+          tc_fence_after();
+          const float a_s = sa_ring[j * BLOCK_M + row];
+          const float* sbg = sb_s + (g - kbeg);
+#pragma unroll
+          for (int c0 = 0; c0 < NCH; c0 += LDS_PER_WAIT) {
+            uint32_t v[LDS_PER_WAIT][32];
+#pragma unroll
+            for (int u = 0; u < LDS_PER_WAIT; ++u)
+              tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * BN + h * HALF + (c0 + u) * 32),
+                                 v[u]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < LDS_PER_WAIT; ++u) {
+              const int col = h * HALF + (c0 + u) * 32;
+              // the 32 columns lie in one 128-column B scale block
+              const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                acc[(c0 + u) * 32 + i] = fmaf(__uint_as_float(v[u][i]), sc, acc[(c0 + u) * 32 + i]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(L::T_EMPTY + b));
+            mbar_arrive(bar(L::SA_EMPTY + j));
+          }
+          if (++b == 2) { b = 0; bph ^= 1; }
+          if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+        }
+      }
+      if constexpr (!SPLIT) {
+        // ------------------------------------ epilogue: bf16 via TMA store --
+        bool zero_row = false;  // contiguous form: padding rows (m_indices = -1) are +0
+        if constexpr (MODE == kContiguous) {
+          if (T.skip) {
+            zero_row = true;
+            if (T.skip == 2 && pt == 0) raise_status(p, ST_EXPERT_RANGE);
+          } else {
+            const int id = __ldg(p.m_indices + T.m0 + row);
+            if (id != T.e) {
+              zero_row = true;
+              if (id >= 0) raise_status(p, ST_EXPERT_RANGE);  // block mixes two experts
+            }
+          }
+        }
+        if (pt == 0) bulk_wait_group_read0();  // the previous store has read the staging tile
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+        // staging: BN/32 chunks of [128 rows x 64 B], 64-byte swizzle (16-byte
+        // unit u of row r sits at unit u ^ ((r >> 1) & 3)), as the store's
+        // tensor map expects
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const uint32_t rbase = out_s + (h * NCH + c) * (BLOCK_M * 64) + row * 64;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int o = c * 32 + u * 8;
+            uint32_t w0 = pack_bf16x2(acc[o + 0], acc[o + 1]);
+            uint32_t w1 = pack_bf16x2(acc[o + 2], acc[o + 3]);
+            uint32_t w2 = pack_bf16x2(acc[o + 4], acc[o + 5]);
+            uint32_t w3 = pack_bf16x2(acc[o + 6], acc[o + 7]);
+            if (zero_row) w0 = w1 = w2 = w3 = 0u;
+            st_shared_v4(rbase + ((u ^ ((row >> 1) & 3)) << 4), w0, w1, w2, w3);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+        if (MODE != kMasked || T.rows == BLOCK_M) {
+          // the store clips at the tensor's bounds (M rows, N columns)
+          if (pt == 0 && !*abort_flag) {
+            for (int cc = 0; cc < BN / 32; ++cc)
+              if (T.n0 + cc * 32 < p.N)
+                tma_store_3d(&tmD, out_s + cc * (BLOCK_M * 64), T.n0 + cc * 32, T.m0, T.z);
+            bulk_commit_group();
+          }
+        } else if (!*abort_flag) {
+          // masked form, last tile of a group: rows >= masked_m[g] keep what D held
+          constexpr int UPR = BN / 8;  // 16-byte units per row
+          for (int i = pt; i < T.rows * UPR; i += 32 * NUM_PROMO_WARPS) {
+            const int r = i / UPR, cu = i - r * UPR;
+            const int n = T.n0 + cu * 8;
+            if (n < p.N) {
+              const uint32_t src = out_s + (cu >> 2) * (BLOCK_M * 64) + r * 64 +
+                                   (((cu & 3) ^ ((r >> 1) & 3)) << 4);
+              const uint4 w = ld_shared_v4(src);
+              *reinterpret_cast<uint4*>(
+                  p.D + (static_cast<size_t>(T.z) * p.M + T.m0 + r) * p.N + n) = w;
+            }
+          }
+        }
+      } else {
+        // ------------- epilogue: K split over the cluster, DSMEM reduction --
+        // fp32 partial [128 rows][BN], 16-byte unit cu of row r stored at unit
+        // cu ^ (r & 7) (conflict-free row-per-thread writes, row-wise reads)
+        wait_bar<true>(bar(L::RED_EMPTY), (k_iter & 1) ^ 1, abort_flag, p);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cu = (h * HALF + c * 32) / 4 + u;
+            const int o = c * 32 + u * 4;
+            st_shared_v4(out_s + row * (BN * 4) + ((cu ^ (row & 7)) << 4), __float_as_uint(acc[o]),
+                         __float_as_uint(acc[o + 1]), __float_as_uint(acc[o + 2]),
+                         __float_as_uint(acc[o + 3]));
+          }
+        }
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+        if (pt == 0) {
+          fence_acq_rel_cluster();
+          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::RED_FULL), r);
+        }
+        wait_bar<true>(bar(L::RED_FULL), k_iter & 1, abort_flag, p);
+        __syncwarp();
+        // this CTA sums rows [r0, r1) of all S partials, in rank order
+        const int R = (BLOCK_M + S - 1) / S;
+        const int r0 = static_cast<int>(crank) * R;
+        const int r1 = min(BLOCK_M, r0 + R);
+        constexpr int UPR = BN / 4;
+        for (int i = pt; i < max(0, r1 - r0) * UPR; i += 32 * NUM_PROMO_WARPS) {
+          const int rr = r0 + i / UPR, cu = i % UPR;
+          const int m = T.m0 + rr, n = T.n0 + cu * 4;
+          if (m < p.M && n < p.N) {
+            const uint32_t off = out_s + rr * (BN * 4) + ((cu ^ (rr & 7)) << 4);
+            float4 sum = ld_cluster_f4(map_cluster(off, 0));
+            for (int r = 1; r < S; ++r) {
+              const float4 v = ld_cluster_f4(map_cluster(off, r));
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            if (!*abort_flag) {
+              uint2 w;
+              w.x = pack_bf16x2(sum.x, sum.y);
+              w.y = pack_bf16x2(sum.z, sum.w);
+              *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(m) * p.N + n) = w;
+            }
+          }
+        }
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+        if (pt == 0)
+          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::RED_EMPTY), r);
+      }
+    }  // tile loop
+    if (SPLIT && k_iter > 0) {
+      // the other CTAs must be done reading this CTA's last partial
+      wait_bar<true>(bar(L::RED_EMPTY), (k_iter & 1) ^ 1, abort_flag, p);
+    }
+    if (pt == 0) bulk_wait_group0();
+    __syncwarp();
+  }
+
+  // ----------------------------------------------------------- teardown --
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+  if (SPLIT) cluster_sync();
+}
+
+}  // namespace dgk

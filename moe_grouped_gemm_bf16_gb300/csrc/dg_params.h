@@ -1,0 +1,48 @@
+// Launch parameters shared by the host launcher and the kernels.
+#pragma once
+#include <cstdint>
+
+namespace dgk {
+
+// Which form of the GEMM a launch computes (DeepGEMM, es.news.hada.io/topic?id=19459,
+// "Dense y Grouped GEMM").
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+
+constexpr int BLOCK_M = 128;  // rows of A per tile (one tcgen05 M=128 MMA)
+constexpr int BLOCK_K = 128;  // one K group: the granularity of both scale factors
+constexpr int NUM_THREADS = 384;  // warpgroup 0: warp 0 TMA, warp 1 MMA; warpgroups 1-2: promotion
+constexpr int NUM_PROMO_WARPS = 8;
+constexpr int SA_SLOTS = 8;   // depth of the activation-scale ring
+constexpr int MAX_GROUPS_MASKED = 1024;
+constexpr int MAX_KB = 512;   // K <= 65536
+
+// Device status word values (first error wins).
+constexpr unsigned int ST_OK = 0;
+constexpr unsigned int ST_TIMEOUT = 7;      // an mbarrier wait gave up
+constexpr unsigned int ST_MASK_RANGE = 8;   // masked_m[g] outside [0, max_m]; clamped
+constexpr unsigned int ST_EXPERT_RANGE = 9; // m_indices out of range or a block mixes experts
+
+// Debug flags (tests of the failure path only).
+constexpr unsigned int DBG_SKIP_PRODUCER = 1u;  // the TMA warp issues nothing
+
+struct Params {
+  int M;           // dense: rows of A/D; contiguous: M_total; masked: max_m
+  int N;
+  int K;
+  int kb;          // K / 128
+  int nb;          // ceil(N / 128): B scale blocks per group
+  int num_groups;  // experts (grouped) or 1
+  int num_m_blocks;  // dense: ceil(M/128); contiguous: M_total/128; masked: computed on device
+  int num_n_blocks;  // ceil(N / BLOCK_N)
+  int raster_m;      // M blocks per raster band
+  int split_k;       // CTAs per cluster, each taking a slice of the K groups
+  const float* sb;             // [G][nb][kb]
+  const int32_t* m_indices;    // contiguous: [M_total]
+  const int32_t* masked_m;     // masked: [G]
+  uint16_t* D;                 // bf16 output, [M][N] or [G][max_m][N]
+  unsigned int* status;        // device status word
+  unsigned long long timeout_ns;
+  unsigned int debug_flags;
+};
+
+}  // namespace dgk

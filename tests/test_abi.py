@@ -1,0 +1,152 @@
+"""The C-ABI library on the host: it loads, exports what include/dg.h declares,
+and rejects bad arguments before launching anything.  No GPU needed: argument
+errors are found before the library touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_grouped_gemm_bf16_gb300 as dg
+from moe_grouped_gemm_bf16_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return dg.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    decl = declared_functions()
+    assert len(decl) >= 14
+    for name in decl:
+        assert hasattr(L, name), name
+    assert sorted(decl) == sorted(dg.EXPORTED_SYMBOLS)
+
+
+# a fake, 16-byte aligned "device" address: never dereferenced by these tests
+P = 0x10000
+
+
+def _dense(**kw):
+    a = dict(A=P, sa=P, ld_sa=128, B=P, sb=P, D=P, M=128, N=256, K=512)
+    a.update(kw)
+    return a
+
+
+def status_of(fn, **kw):
+    try:
+        fn(**kw)
+    except dg.DGError as e:
+        return e.status
+    return 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(A=None), 1),
+    (dict(D=None), 1),
+    (dict(M=-1), 1),
+    (dict(K=500), 2),
+    (dict(K=0), 2),
+    (dict(K=128 * 513), 2),
+    (dict(N=200), 2),
+    (dict(N=8), 2),
+    (dict(A=P + 8), 3),
+    (dict(D=P + 2), 3),
+    (dict(sa=P + 4), 3),
+    (dict(ld_sa=130), 3),
+    (dict(ld_sa=64), 1),
+])
+def test_dense_argument_errors(L, kw, code):
+    assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(**kw)) == code
+    assert dg.lib().dg_last_error_string().decode() != ""
+
+
+def test_empty_problem_is_a_noop(L):
+    # M = 0: nothing to compute, no device needed
+    assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(M=0)) == 0
+
+
+def test_grouped_argument_errors(L):
+    c = dict(A=P, sa=P, ld_sa=256, B=P, sb=P, D=P, m_indices=P, M_total=256, N=256, K=512,
+             num_groups=4)
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous, **{**c, "M_total": 200,
+                                                                        "ld_sa": 200}) == 2
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous, **{**c, "num_groups": 0}) == 1
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous, **{**c, "m_indices": None}) == 1
+    m = dict(A=P, sa=P, ld_sa=128, B=P, sb=P, D=P, masked_m=P, num_groups=4, max_m=128, N=256,
+             K=512, expected_m=64)
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked, **{**m, "num_groups": 1025}) == 1
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked, **{**m, "masked_m": None}) == 1
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked, **{**m, "ld_sa": 100}) == 1
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked, **{**m, "max_m": 0}) == 0
+
+
+def test_valid_call_without_device_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense()) in (4,)
+
+
+def test_utilities(L):
+    assert dg.get_mk_alignment_for_contiguous_layout() == 128
+    # fp32 scales: 4 elements per 16 bytes
+    assert [dg.get_tma_aligned_size(m, 4) for m in (0, 1, 4, 5, 64, 130)] == [0, 4, 4, 8, 64, 132]
+    assert dg.get_tma_aligned_size(7, 2) == 8
+    assert dg.get_tma_aligned_size(17, 1) == 32
+    assert dg.get_tma_aligned_size(-1, 4) == -1
+    with pytest.raises(dg.DGError):
+        dg.set_num_sms(-3)
+    dg.set_wait_timeout_ns(0)
+
+
+def test_sm_fill_golden(L):
+    """The pages' unaligned-block-size example: tile counts (one tile per SM)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "sm_fill_example.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].split()
+            if line:
+                rows.append([int(x) for x in line])
+    assert len(rows) == 2
+    for M, N, bm, bn, tiles in rows:
+        assert dg.num_output_tiles(M, N, bm, bn) == tiles
+
+
+def test_plan_config_heuristic(L):
+    # decode: few output tiles -> the K groups are split over a cluster
+    cfg = dg.plan_config(0, 64, 2112, 7168, 1, 152)
+    assert cfg["split_k"] > 1 and cfg["grid"] <= 152 and cfg["block_m"] == 128
+    # prefill: enough tiles -> no split, wide tiles
+    cfg = dg.plan_config(0, 4096, 7168, 7168, 1, 152)
+    assert cfg["split_k"] == 1 and cfg["grid"] <= 152
+    assert cfg["num_tiles"] == 32 * ((7168 + cfg["block_n"] - 1) // cfg["block_n"])
+    for kind, m, g in ((1, 32768, 4), (2, 256, 8)):
+        cfg = dg.plan_config(kind, m, 4096, 7168, g, 152)
+        assert cfg["split_k"] == 1 and cfg["smem_bytes"] <= 232448
+    with pytest.raises(dg.DGError):
+        dg.plan_config(0, 64, 2112, 7000, 1, 152)
+
+
+def test_force_config_hook(L):
+    try:
+        dg.debug_force_config(256, 0)
+        assert dg.plan_config(0, 4096, 4096, 1024, 1, 152)["block_n"] == 256
+        dg.debug_force_config(128, 4)
+        cfg = dg.plan_config(0, 128, 4096, 1024, 1, 152)
+        assert (cfg["block_n"], cfg["split_k"]) == (128, 4)
+        with pytest.raises(dg.DGError):
+            dg.debug_force_config(128, 9)
+    finally:
+        dg.debug_force_config(0, 0)

@@ -1,0 +1,144 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs small
+enough for the oracle to finish in seconds, spanning several tiles and ragged
+tails, through the C ABI.  Every kernel instance is exercised by forcing its
+configuration, besides the heuristic's own choice."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_bf16_gb300 as dg
+import oracle
+import workloads as W
+from moe_grouped_gemm_bf16_gb300 import _build
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+ORC = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    global ORC
+    _build.build()
+    ORC = oracle.Oracle()
+    torch.cuda.init()
+    yield
+    dg.debug_force_config(0, 0)
+
+
+def dense_ref(p):
+    return ORC.gemm_nt(p["A"], p["sa"], p["B"], p["sb"])
+
+
+# (block_n, split_k): every dense instance, plus the heuristic (0, 0)
+DENSE_CONFIGS = [(0, 0), (128, 1), (256, 1), (128, 2), (128, 3), (128, 4), (128, 8)]
+
+
+@pytest.mark.parametrize("cfg", DENSE_CONFIGS, ids=lambda c: f"bn{c[0]}_s{c[1]}")
+def test_dense_tiny_config(cfg):
+    """The small dense case: M=128, N=256, K=512."""
+    p = W.dense_problem(128, 256, 512, seed=1000)
+    with U.forced_config(*cfg):
+        got = U.run_dense(p)
+    U.assert_close(got, dense_ref(p), f"dense 128x256x512 cfg={cfg}")
+
+
+RAGGED = [
+    (1, 16, 128),        # one row, one column block, one K group
+    (64, 144, 640),      # decode-sized M, ragged N tail, 5 K groups
+    (200, 400, 384),     # ragged M and N
+    (333, 2112, 256),    # the 2112 width: last B scale block is 64 rows
+    (512, 528, 1024),    # several M and N tiles
+    (130, 272, 128 * 9),  # K groups not divisible by the split
+]
+
+
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("cfg", [(0, 0), (128, 1), (256, 1), (128, 3)],
+                         ids=lambda c: f"bn{c[0]}_s{c[1]}")
+def test_dense_ragged(shape, cfg):
+    M, N, K = shape
+    p = W.dense_problem(M, N, K, seed=M * 7 + N + K)
+    with U.forced_config(*cfg):
+        got = U.run_dense(p)
+    U.assert_close(got, dense_ref(p), f"dense {shape} cfg={cfg}")
+
+
+def test_dense_more_splits_than_groups():
+    """split_k = 8 with only 2 K groups: six CTAs of each cluster get no K
+    group and add zeros."""
+    p = W.dense_problem(96, 256, 256, seed=5)
+    with U.forced_config(128, 8):
+        got = U.run_dense(p)
+    U.assert_close(got, dense_ref(p), "split 8 > K groups")
+
+
+def test_dense_special_values():
+    """Integer-valued codes and power-of-two scales: the exact answer is an
+    integer, which bf16 holds exactly below 256 (sparse inputs)."""
+    rng = np.random.default_rng(3)
+    M, N, K = 256, 384, 512
+    A = np.where(rng.random((M, K)) < 0.02, 0x38, 0).astype(np.uint8)  # 1.0 or 0
+    B = np.where(rng.random((N, K)) < 0.05, 0xC0, 0).astype(np.uint8)  # -2.0 or 0
+    sa = np.ones((K // 128, M), np.float32)
+    sb = np.ones(((N + 127) // 128, K // 128), np.float32)
+    p = dict(A=A, sa=sa, B=B, sb=sb, M=M, N=N, K=K)
+    got = U.run_dense(p)
+    want = dense_ref(p)
+    assert np.array_equal(got, want)
+
+
+def test_dense_repeat_is_deterministic():
+    p = W.dense_problem(64, 2112, 1024, seed=9)
+    a = U.run_dense(p)
+    b = U.run_dense(p)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("cfg", [(0, 0), (128, 1), (256, 1)], ids=lambda c: f"bn{c[0]}")
+def test_contiguous_small(cfg):
+    p = W.contiguous_problem(3, 272, 384, 1, 300, seed=31)
+    with U.forced_config(*cfg):
+        got = U.run_contiguous(p)
+    want = ORC.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], p["m_indices"])
+    pad = p["m_indices"] < 0
+    assert pad.any()
+    assert np.all(got[pad] == 0), "padding rows must be +0"
+    U.assert_close(got[~pad], want[~pad], f"contiguous cfg={cfg}")
+
+
+def test_contiguous_all_padding_block():
+    """A 128-row block whose first row is -1 is all padding."""
+    p = W.contiguous_problem(2, 128, 256, 5, 100, seed=33)
+    M = p["M"]
+    # append a whole padding block
+    p = dict(p)
+    p["A"] = np.concatenate([p["A"], W.random_codes((128, p["K"]), 1)])
+    sa = np.ones((p["K"] // 128, W.tma_aligned_ld(M + 128)), np.float32)
+    sa[:, :M] = p["sa"][:, :M]
+    p["sa"] = sa
+    p["m_indices"] = np.concatenate([p["m_indices"], np.full(128, -1, np.int32)])
+    p["M"] = M + 128
+    got = U.run_contiguous(p)
+    want = ORC.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], p["m_indices"])
+    assert np.all(got[M:] == 0)
+    pad = p["m_indices"] < 0
+    U.assert_close(got[~pad], want[~pad], "contiguous with padding block")
+
+
+@pytest.mark.parametrize("cfg", [(0, 0), (128, 1), (256, 1)], ids=lambda c: f"bn{c[0]}")
+def test_masked_small(cfg):
+    p = W.masked_problem(5, 300, 400, 384, 100, seed=41)
+    # edge counts: an empty group, exactly one tile, the full max_m
+    mm = p["masked_m"].copy()
+    mm[0], mm[1], mm[2] = 0, 128, 300
+    p["masked_m"] = mm
+    with U.forced_config(*cfg):
+        got = U.run_masked(p)
+    init = np.full(got.shape, W.BF16_SENTINEL, np.uint16)
+    want = ORC.grouped_masked(p["A"], p["sa"], p["B"], p["sb"], mm, init)
+    for g in range(p["G"]):
+        v = int(mm[g])
+        assert np.all(got[g, v:] == W.BF16_SENTINEL), f"group {g}: rows past masked_m written"
+        U.assert_close(got[g, :v], want[g, :v], f"masked group {g}")
