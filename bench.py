@@ -1,0 +1,576 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 fine-grained-scaled GEMM library on GB300.
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                 [--workload dense_decode|dense_prefill|grouped_contiguous|grouped_masked]
+                 [--case I]`
+
+Prints one JSON line.  A step is one pass of the GEMM over every case of the
+workload (default: the dense decode sweep, M in {64, 128} x six (N, K) pairs of
+the DeepSeek-V3/R1 inference shapes), with all inputs resident in HBM and the
+step captured once in a CUDA graph.  `value` is algorithmic HBM bytes per
+second (GB/s) over the K timed steps; `e2e` is the same metric through the C
+ABI with the inputs copied from pinned host memory and the outputs copied back
+inside every step.
+
+`--impl reference` times the CPU oracle (the plain C reference) on this
+machine's host cores instead, on a bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank runs the whole workload on its own GPU
+(replicas, no collective on the data path); timing is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "FP8 block-scaled GEMM TFLOPS & HBM GB/s, % of GB300 FP8/HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+HBM_BOUND = ("dense_decode",)
+
+
+# ------------------------------------------------------------- workloads ---
+class Case:
+    """One GEMM call of a workload: its host inputs and algorithmic counts."""
+
+    def __init__(self, kind, prob, label):
+        self.kind = kind
+        self.p = prob
+        self.label = label
+        K = prob["K"]
+        kb = K // 128
+        N = prob["N"]
+        nb = (N + 127) // 128
+        if kind == "dense":
+            mv, gu = prob["M"], 1
+        elif kind == "contiguous":
+            mv, gu = int((prob["m_indices"] >= 0).sum()), prob["G"]
+        else:
+            mv, gu = int(prob["masked_m"].sum()), int((prob["masked_m"] > 0).sum())
+        self.m_valid = mv
+        # algorithmic work counts valid rows only (padding and masked rows excluded)
+        self.flops = 2.0 * mv * N * K
+        self.bytes = mv * K + gu * N * K + 4 * mv * kb + 4 * gu * nb * kb + 2 * mv * N
+
+
+def make_cases(name, only=None):
+    cfg = W.CONFIGS[name]
+    out = []
+    if cfg["kind"] == "dense":
+        for (M, N, K) in cfg["cases"]:
+            out.append(("dense", lambda M=M, N=N, K=K: W.dense_problem(M, N, K, seed=cfg["seed"]),
+                        f"{M}x{N}x{K}"))
+    elif cfg["kind"] == "contiguous":
+        for (N, K) in cfg["nk"]:
+            out.append(("contiguous", lambda N=N, K=K: W.contiguous_problem(
+                cfg["groups"], N, K, *cfg["m_range"], seed=cfg["seed"]),
+                f"G{cfg['groups']}x{N}x{K}"))
+    else:
+        for G in cfg["groups"]:
+            for (N, K) in cfg["nk"]:
+                out.append(("masked", lambda G=G, N=N, K=K: W.masked_problem(
+                    G, cfg["max_m"], N, K, cfg["expected_m"], seed=cfg["seed"] + G),
+                    f"G{G}x{cfg['max_m']}x{N}x{K}"))
+    if only is not None:
+        out = [out[only]]
+    return [Case(kind, make(), label) for kind, make, label in out]
+
+
+def describe(name):
+    cfg = W.CONFIGS[name]
+    if name == "dense_decode":
+        return ("dense decode sweep: M in {64,128} x (N,K) in "
+                + ",".join(f"({n},{k})" for n, k in W.DENSE_NK))
+    if name == "dense_prefill":
+        return "dense prefill sweep: M=4096 x (N,K) in " + ",".join(
+            f"({n},{k})" for n, k in W.DENSE_NK)
+    if name == "dense_tiny":
+        return "dense M=128, N=256, K=512"
+    if name == "grouped_contiguous":
+        return (f"contiguous M-grouped: {cfg['groups']} experts, m_e~U[{cfg['m_range'][0]},"
+                f"{cfg['m_range'][1]}] padded to 128, (N,K) in {cfg['nk']}")
+    return (f"masked M-grouped: G in {cfg['groups']}, max_m={cfg['max_m']}, "
+            f"masked_m~U[1,{2 * cfg['expected_m']}], (N,K) in {cfg['nk']}")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_grouped_gemm_bf16_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU arm ---
+class DeviceCase:
+    """A case's tensors resident on the GPU and the library call on them."""
+
+    def __init__(self, c, torch, dg):
+        self.c = c
+        self.dg = dg
+        p = c.p
+        dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+        self.A, self.sa, self.B, self.sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])
+        self.idx = None
+        if c.kind == "dense":
+            self.D = torch.zeros((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda")
+        elif c.kind == "contiguous":
+            self.idx = dev(p["m_indices"])
+            self.D = torch.zeros((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda")
+        else:
+            self.idx = dev(p["masked_m"])
+            self.D = torch.zeros((p["G"], p["max_m"], p["N"]), dtype=torch.bfloat16,
+                                 device="cuda")
+        self.inputs = [self.A, self.sa, self.B, self.sb] + (
+            [self.idx] if self.idx is not None else [])
+
+    def call(self, stream):
+        p, dg = self.c.p, self.dg
+        if self.c.kind == "dense":
+            dg.gemm_fp8_fp8_bf16_nt(self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D,
+                                    p["M"], p["N"], p["K"], stream)
+        elif self.c.kind == "contiguous":
+            dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, self.idx, p["M"],
+                p["N"], p["K"], p["G"], stream)
+        else:
+            em = W.CONFIGS["grouped_masked"]["expected_m"]
+            dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, self.idx, p["G"],
+                p["max_m"], p["N"], p["K"], em, stream)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def run_ours(args):
+    import torch
+
+    import moe_grouped_gemm_bf16_gb300 as dg
+    from moe_grouped_gemm_bf16_gb300 import _build
+
+    world, rank, local, pg = dist_setup()
+    torch.cuda.set_device(local)
+    _build.build()
+    dg.lib()
+    cases = make_cases(args.workload, args.case)
+    dcs = [DeviceCase(c, torch, dg) for c in cases]
+    stream = torch.cuda.Stream()
+    step_bytes = sum(c.bytes for c in cases)
+    step_flops = sum(c.flops for c in cases)
+    footprint = sum(sum(t.numel() * t.element_size() for t in d.inputs) +
+                    d.D.numel() * d.D.element_size() for d in dcs)
+
+    with torch.cuda.stream(stream):
+        # eager warm-up (device set-up, occupancy queries), then graph capture
+        for _ in range(2):
+            for d in dcs:
+                d.call(stream.cuda_stream)
+        stream.synchronize()
+        if dg.get_device_status(stream.cuda_stream) != 0:
+            raise RuntimeError("device status set during warm-up")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for d in dcs:
+                d.call(stream.cuda_stream)
+        for _ in range(args.warmup):
+            graph.replay()
+        stream.synchronize()
+
+        steps = args.steps
+        if steps is None:
+            # default: a timed region of about two seconds
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                graph.replay()
+            e1.record(stream)
+            stream.synchronize()
+            per = e0.elapsed_time(e1) / 5.0
+            steps = int(max(20, min(20000, 2000.0 / max(per, 1e-3))))
+            steps = int(max_over_ranks(pg, steps))
+
+        sampler = ClockSampler(local) if rank == 0 else None
+        barrier(pg)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        t1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        barrier(pg)
+        ms = max_over_ranks(pg, t0.elapsed_time(t1))
+        status = dg.get_device_status(stream.cuda_stream)
+        if status != 0:
+            raise RuntimeError(f"device status {status} after the timed region")
+
+    ms_per_step = ms / steps
+    value = world * step_bytes * steps / (ms / 1e3) / 1e9
+    tflops = world * step_flops * steps / (ms / 1e3) / 1e12
+
+    per_case = per_case_cold(dcs, torch, stream) if (rank == 0 and not args.quick) else None
+    e2e = run_e2e(dcs, cases, torch, stream, min(steps, args.e2e_steps), pg, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases)
+
+    if rank != 0:
+        return None
+    hbm, bf16, _bf16_sus, src = measured_peaks()
+    launches_per_step = len(dcs)
+    avg_launch_s = (ms_per_step / 1e3) / launches_per_step
+    if args.workload in HBM_BOUND:
+        achieved = step_bytes / launches_per_step / avg_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": recorded_traffic(args.workload),
+                "peak_source": ("measured HBM copy, MEASURED_PEAKS.json hbm_gbs"
+                                if src == "measured" else "fallback 6.8 TB/s")}
+    else:
+        # dense FP8 tensor peak = bf16 measured x 2 (nominal ratio 4.5 / 2.25 PFLOP/s)
+        fp8_peak = 2.0 * bf16
+        achieved = step_flops / launches_per_step / avg_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                "traffic": recorded_traffic(args.workload),
+                "peak_source": (f"{src} bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)")}
+    desc = describe(args.workload)
+    if args.case is not None:
+        desc += f" (case {args.case} only: {cases[0].label})"
+    big = footprint > 2 * L2_BYTES
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1), 1x128 / 128x128 fp32-scaled e4m3)",
+        "config": {"workload": desc, "cases": len(cases),
+                   "launch": "one CUDA graph per step (all cases), inputs resident in HBM",
+                   "l2": (f"inputs larger than L2: step footprint {footprint / 1e6:.0f} MB vs "
+                          f"129 MB L2; each case's buffers are evicted by the other cases "
+                          f"before it runs again") if big else
+                         (f"step footprint {footprint / 1e6:.0f} MB: NOT larger than L2, "
+                          f"repeats may hit L2"),
+                   "parallelism": f"replicas x{world}"},
+        "tflops": round(tflops, 1),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": steps * launches_per_step,
+        "clocks": clocks,
+        "cases": per_case,
+    }
+
+
+def per_case_cold(dcs, torch, stream, reps=5):
+    """Per-case kernel time with a cold L2: a 256 MB buffer is written before
+    every launch and only the GEMM launch sits between the events.  Runs after
+    the timed region; reported as detail."""
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    out = []
+    with torch.cuda.stream(stream):
+        for d in dcs:
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                d.call(stream.cuda_stream)
+                e1.record(stream)
+                stream.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            us = statistics.median(ts)
+            out.append({"case": d.c.label, "us": round(us, 2),
+                        "gbs": round(d.c.bytes / (us * 1e-6) / 1e9, 1),
+                        "tflops": round(d.c.flops / (us * 1e-6) / 1e12, 1)})
+    del flush
+    return out
+
+
+def run_e2e(dcs, cases, torch, stream, steps, pg, world):
+    """The same metric through the C ABI, with every step's inputs copied from
+    pinned host memory and every output read back to the host."""
+    steps = max(3, int(steps))
+    host_in = [[t.cpu().pin_memory() for t in d.inputs] for d in dcs]
+    host_out = [torch.empty(d.D.shape, dtype=d.D.dtype).pin_memory() for d in dcs]
+    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            for d, hs, ho in zip(dcs, host_in, host_out):
+                for dev_t, h in zip(d.inputs, hs):
+                    dev_t.copy_(h, non_blocking=True)
+                d.call(stream.cuda_stream)
+                ho.copy_(d.D, non_blocking=True)
+        stream.synchronize()
+
+    one_step()
+    barrier(pg)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    dt = max_over_ranks(pg, time.perf_counter() - t0)
+    step_bytes = sum(c.bytes for c in cases)
+    return {"value": round(world * step_bytes * steps / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4)}
+
+
+# -------------------------------------------------------- CPU oracle arm ---
+def _oracle_sample(orc, c, rows, ncols, threads):
+    """Time the oracle on `rows` output rows x the first `ncols` output columns
+    of case c.  Returns (seconds, sampled output elements, output elements of
+    the whole case)."""
+    p = c.p
+    ncols = min(ncols, p["N"])
+    nbs = (ncols + 127) // 128
+    if c.kind == "dense":
+        r = np.linspace(0, p["M"] - 1, num=min(rows, p["M"])).astype(np.int64)
+        t = time.perf_counter()
+        orc.gemm_nt_rows(p["A"], p["sa"], p["B"][:ncols], p["sb"][:nbs], r, nthreads=threads)
+        return time.perf_counter() - t, r.size * ncols, c.m_valid * p["N"]
+    if c.kind == "contiguous":
+        valid = np.nonzero(p["m_indices"] >= 0)[0]
+        r = valid[np.linspace(0, valid.size - 1, num=min(rows, valid.size)).astype(np.int64)]
+        t = time.perf_counter()
+        orc.grouped_contiguous(p["A"], p["sa"], p["B"][:, :ncols], p["sb"][:, :nbs],
+                               p["m_indices"], rows=r, nthreads=threads)
+        return time.perf_counter() - t, r.size * ncols, c.m_valid * p["N"]
+    G = p["G"]
+    per = max(1, rows // G)
+    secs, done = 0.0, 0
+    for g in range(G):
+        v = int(p["masked_m"][g])
+        if v == 0:
+            continue
+        r = np.linspace(0, v - 1, num=min(per, v)).astype(np.int64)
+        t = time.perf_counter()
+        orc.gemm_nt_rows(p["A"][g], p["sa"][g], p["B"][g][:ncols], p["sb"][g][:nbs], r,
+                         nthreads=threads)
+        secs += time.perf_counter() - t
+        done += r.size * ncols
+    return secs, done, c.m_valid * p["N"]
+
+
+def cpu_baseline(cases):
+    """The oracle as it stands, on this host's cores, on a bounded sample of
+    every case: `cores` whole output rows per case; the time is scaled to the
+    whole case by the ratio of output elements."""
+    import oracle
+    orc = oracle.Oracle()
+    cores = len(os.sched_getaffinity(0))
+    t_full, wall, total_bytes = 0.0, 0.0, 0
+    for c in cases:
+        secs, done, full = _oracle_sample(orc, c, cores, c.p["N"], cores)
+        wall += secs
+        t_full += secs * full / done
+        total_bytes += c.bytes
+    return {"value": round(total_bytes / t_full / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{cores} whole output rows per case ({len(cases)} cases); time scaled "
+                      f"to the whole case by output elements; {wall:.1f} s wall",
+            "seconds": round(wall, 2)}
+
+
+def run_reference(args):
+    """The CPU oracle timed on this host's cores; step i samples case i mod n,
+    each step sized so the whole run takes about two minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.Oracle()
+    cores = len(os.sched_getaffinity(0))
+    cases = make_cases(args.workload, args.case)
+    steps = args.steps if args.steps is not None else 2 * len(cases)
+    warm = args.warmup
+    budget = 120.0 / max(1, steps + warm)
+    s, done, _ = _oracle_sample(orc, cases[0], cores, 128, cores)
+    rate = done * cases[0].p["K"] / max(s, 1e-6)  # output-element MACs per second
+    t_full, bytes_sum, wall = 0.0, 0, 0.0
+    for i in range(warm + steps):
+        c = cases[i % len(cases)]
+        rows = min(cores, c.m_valid)
+        cols = int(budget * rate / (rows * c.p["K"]))
+        cols = max(16, min(c.p["N"], cols // 16 * 16))
+        secs, done, full = _oracle_sample(orc, c, rows, cols, cores)
+        if i >= warm:
+            wall += secs
+            t_full += secs * full / done
+            bytes_sum += c.bytes
+    value = bytes_sum / t_full / 1e9
+    sample = (f"per step one case (round robin over {len(cases)}), {cores} output rows x up to "
+              f"all columns (sized for a ~2 minute run); time scaled to the whole case by "
+              f"output elements")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": round(wall / steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), 1x128 / 128x128 fp32-scaled e4m3)",
+        "config": {"workload": describe(args.workload), "cases": len(cases),
+                   "parallelism": "host cores (OpenMP over output rows)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about two seconds of steps)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.CONFIGS), default="dense_decode")
+    ap.add_argument("--case", type=int, default=None,
+                    help="run only case I of the workload (profiling one shape)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the per-case cold-L2 detail (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.impl == "ours" and args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

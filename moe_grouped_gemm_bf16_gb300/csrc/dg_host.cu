@@ -118,7 +118,9 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;
     const int s_lo = in.split ? 2 : 1;
-    const int s_hi = in.split ? std::min(kMaxCluster, kb) : 1;
+    // the heuristic splits no finer than one K group per CTA; a forced split
+    // may (the CTAs without a K group add zeros)
+    const int s_hi = in.split ? (force_split > 0 ? kMaxCluster : std::min(kMaxCluster, kb)) : 1;
     for (int S = s_lo; S <= s_hi; ++S) {
       if (force_split > 0 && S != force_split) continue;
       if (force_split == 0 && force_bn > 0 && in.split) {
