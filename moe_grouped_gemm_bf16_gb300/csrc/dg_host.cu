@@ -134,15 +134,20 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
       const long long c = std::max(1, cap(i, in, S, smem));
       const long long waves = cdiv(tiles, c);
       const long long kper = cdiv(kb, S);
-      // bytes each CTA streams per K group, in units of 128 B rows: A (128) + B (BN)
-      double cost = (double)waves * ((double)kper * (128 + in.block_n) +
-                                     (S > 1 ? 4.0 * (128 + in.block_n) : 0.0) + 8.0 * 128);
+      // Per wave: the K groups each CTA streams, weighted by the bytes of one
+      // K group (A: 128 rows, B: BN rows), plus a fixed cost per wave (first
+      // load latency, prologue, epilogue) worth about 12 K groups, plus the
+      // cluster reduction when the K groups are split.
+      const double unit = 128.0 + in.block_n;
+      double cost = (double)waves * (((double)kper + 12.0 + (S > 1 ? 4.0 : 0.0)) * unit);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.inst = i;
         best.split = S;
         best.tiles = tiles;
-        best.clusters = (int)std::min<long long>(tiles, c);
+        // the split form runs one cluster per tile (its epilogue reuses the
+        // operand ring); the others are persistent, at most one wave of CTAs
+        best.clusters = in.split ? (int)tiles : (int)std::min<long long>(tiles, c);
         best.smem = smem;
       }
     }

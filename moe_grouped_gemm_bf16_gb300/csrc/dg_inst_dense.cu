@@ -7,7 +7,7 @@ const Instance* instances_dense(int* count) {
   static const Instance table[] = {
       InstanceOf<128, 5, false, kDense>::make(),
       InstanceOf<256, 3, false, kDense>::make(),
-      InstanceOf<128, 4, true, kDense>::make(),
+      InstanceOf<128, 6, true, kDense>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;

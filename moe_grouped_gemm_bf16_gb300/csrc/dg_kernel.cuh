@@ -12,7 +12,7 @@
 //               S-stage ring; the 128 activation scales of the K group into a
 //               separate ring (they are read later, by the promotion warps).
 //   warp 1      allocates tensor memory; one thread issues 4 tcgen05.mma
-//               (K = 32 each) per K group into one of two TMEM accumulators,
+//               (K = 32 each) per K group into one of 2-4 TMEM accumulators,
 //               then commits: the stage goes back to the producer, the
 //               accumulator goes to the promotion warps.
 //   warps 4..11 promotion (two warpgroups): read the group's fp32 partial from TMEM, scale it by
@@ -46,21 +46,26 @@ struct SmemLayout {
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
   static constexpr int SA_OFF = B_OFF + STAGES * B_BYTES;
-  static constexpr int OUT_OFF = SA_OFF + SA_SLOTS * SA_BYTES;
-  // bf16 staging for the TMA store, or the fp32 partial for the split reduction
+  // bf16 staging tile for the TMA store.  With the K split, each cluster
+  // computes one tile, so after its last K group the operand ring is idle and
+  // holds the fp32 partial of the reduction instead.
+  static constexpr int OUT_OFF = SPLIT ? A_OFF : SA_OFF + SA_SLOTS * SA_BYTES;
   static constexpr int OUT_BYTES = SPLIT ? BLOCK_M * BN * 4 : BLOCK_M * BN * 2;
-  static constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
+  static_assert(!SPLIT || OUT_BYTES <= STAGES * (A_BYTES + B_BYTES), "partial must fit the ring");
+  static constexpr int BAR_OFF = SPLIT ? SA_OFF + SA_SLOTS * SA_BYTES : OUT_OFF + OUT_BYTES;
   // barrier indexes
   static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
-                       T_EMPTY = T_FULL + 2, RED_FULL = T_EMPTY + 2, RED_EMPTY = RED_FULL + 1,
+                       T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, RED_EMPTY = RED_FULL + 1,
                        MMA_DONE = RED_EMPTY + 1, NUM_BARS = MMA_DONE + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int DYN_OFF = MISC_OFF + 16;            // sb tile, then masked tables
   static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
-  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                   : (2 * BN <= 256) ? 256 : 512;
+  // TMEM accumulators (K groups the MMA may run ahead of the promotion warps):
+  // as many BN-column buffers as the 512 columns hold, at most 4
+  static constexpr int NBUF = (BN <= 128) ? 4 : 2;
+  static constexpr int TMEM_COLS = (NBUF * BN <= 128) ? 128 : (NBUF * BN <= 256) ? 256 : 512;
 };
 
 // Dynamic shared memory a launch needs (host side too).
@@ -221,7 +226,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(bar(L::SA_FULL + j), 1);
       mbar_init(bar(L::SA_EMPTY + j), NUM_PROMO_WARPS);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < L::NBUF; ++b) {
       mbar_init(bar(L::T_FULL + b), 1);
       mbar_init(bar(L::T_EMPTY + b), NUM_PROMO_WARPS);
     }
@@ -272,6 +277,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const uint32_t tmem_base = misc[0];
   const int num_m_blocks = (MODE == kMasked) ? prefix[p.num_groups] : p.num_m_blocks;
   const int num_tiles = num_m_blocks * p.num_n_blocks;
+  // the split form computes exactly one tile per cluster (the host launches one
+  // cluster per tile); the operand ring is reused by its epilogue
+  const int tile_stride = SPLIT ? num_tiles : num_clusters;
 
   // A 256-column tile needs 128 accumulator registers per promotion thread:
   // move registers from warpgroup 0 (TMA, MMA, two idle warps) to the two
@@ -287,7 +295,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t issued_mask = 0, issued_par = 0, sa_issued_mask = 0, sa_issued_par = 0;
       int s = 0, j = 0;
       uint32_t ph = 0, jph = 0;
-      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      for (int t = cluster_id; t < num_tiles; t += tile_stride) {
         const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
         if (T.skip) continue;
         for (int g = kbeg; g < kend; ++g) {
@@ -325,7 +333,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) {
       int s = 0, b = 0;
       uint32_t ph = 0, bph = 0;
-      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      for (int t = cluster_id; t < num_tiles; t += tile_stride) {
         const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
         if (T.skip) continue;
         for (int g = kbeg; g < kend; ++g) {
@@ -344,7 +352,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mma_commit(bar(L::T_FULL + b));
           }
           if (++s == STAGES) { s = 0; ph ^= 1; }
-          if (++b == 2) { b = 0; bph ^= 1; }
+          if (++b == L::NBUF) { b = 0; bph ^= 1; }
         }
       }
       // nothing issued may still run when the TMEM is freed
@@ -367,7 +375,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t bph = 0, jph = 0;
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
     float acc[HALF];
-    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++k_iter) {
+    for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
       // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
@@ -415,7 +423,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_arrive(bar(L::T_EMPTY + b));
             mbar_arrive(bar(L::SA_EMPTY + j));
           }
-          if (++b == 2) { b = 0; bph ^= 1; }
+          if (++b == L::NBUF) { b = 0; bph ^= 1; }
           if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
         }
       }
@@ -512,11 +520,17 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const int m = T.m0 + rr, n = T.n0 + cu * 4;
           if (m < p.M && n < p.N) {
             const uint32_t off = out_s + rr * (BN * 4) + ((cu ^ (rr & 7)) << 4);
-            float4 sum = ld_cluster_f4(map_cluster(off, 0));
-            for (int r = 1; r < S; ++r) {
-              const float4 v = ld_cluster_f4(map_cluster(off, r));
-              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-            }
+            // issue every rank's load first, then add in rank order
+            float4 v[MAX_SPLIT];
+#pragma unroll
+            for (int r = 0; r < MAX_SPLIT; ++r)
+              if (r < S) v[r] = ld_cluster_f4(map_cluster(off, r));
+            float4 sum = v[0];
+#pragma unroll
+            for (int r = 1; r < MAX_SPLIT; ++r)
+              if (r < S) {
+                sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
+              }
             if (!*abort_flag) {
               uint2 w;
               w.x = pack_bf16x2(sum.x, sum.y);

@@ -15,6 +15,7 @@ constexpr int NUM_PROMO_WARPS = 8;
 constexpr int SA_SLOTS = 8;   // depth of the activation-scale ring
 constexpr int MAX_GROUPS_MASKED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
+constexpr int MAX_SPLIT = 8;  // CTAs per cluster in the K-split form
 
 // Device status word values (first error wins).
 constexpr unsigned int ST_OK = 0;
