@@ -104,6 +104,46 @@ struct Plan {
   int smem = 0;
 };
 
+// Estimated kernel time (us) of one configuration, from measured GB300
+// figures: a 128-deep K group of tcgen05.mma (M=128) takes ~454 cycles for
+// N <= 128 and ~643 cycles for N = 256 (dependent-accumulate floor and tensor
+// throughput); a TMA load round trip under load is ~1.6 us; HBM ~6.5 TB/s.
+double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
+                   int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
+  const double ghz = 2.0;
+  const double t_mma = (in.block_n <= 128 ? 454.0 : 643.0 * in.block_n / 256.0) / (ghz * 1e3);
+  const long long kb = k / 128;
+  const long long kper = cdiv(kb, S);
+  long long ctas, rounds;
+  if (in.split) {
+    // one cluster per tile, as many waves as the resident clusters need
+    rounds = cdiv(tiles, clusters_resident);
+    ctas = std::min<long long>(tiles, clusters_resident) * S;
+  } else {
+    ctas = std::min<long long>(tiles, num_sms);
+    rounds = cdiv(tiles, ctas);  // tiles one persistent CTA computes in turn
+  }
+  const double t_comp = (double)rounds * kper * t_mma;
+  // unique HBM bytes: operands once, output once
+  const double groups = (kind == dgk::kDense) ? 1.0 : (double)num_groups;
+  const double m_all = (kind == dgk::kMasked) ? (double)num_groups * m_rows : (double)m_rows;
+  const double bytes = m_all * k + groups * (double)n * k + 2.0 * m_all * n;
+  // bytes in flight bound the bandwidth a wave can draw
+  const double stage_b = (double)in.block_n * 128.0;
+  const double bw = std::min(6.5e6, (double)ctas * in.stages * stage_b / 1.6);  // bytes/us
+  const double t_mem = bytes / bw;
+  const double fixed = 2.0 + (double)rounds * (S > 1 ? 1.5 : 0.6);
+  // the MMA issue and the loads overlap only in part (measured per-group
+  // cadence: MMA time plus a share of the load wait)
+  return std::max(t_comp, t_mem) + 0.5 * std::min(t_comp, t_mem) + fixed;
+}
+
+bool has_split64(const Table& tab) {
+  for (int i = 0; i < tab.n; ++i)
+    if (tab.p[i].split && tab.p[i].a_rows == 64) return true;
+  return false;
+}
+
 // cap(S): clusters of S CTAs that can be resident at once.
 template <typename Cap>
 Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sms, Cap cap,
@@ -115,8 +155,16 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
   for (int i = 0; i < tab.n; ++i) {
     const Instance& in = tab.p[i];
     if (force_bn > 0 && in.block_n != force_bn) continue;
+    // 64-row A tiles serve M <= 64 only, and are the choice there
+    if (in.a_rows < 128 && m_rows > in.a_rows) continue;
+    if (in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;
+    // the K split is for shapes whose output tiles cannot fill the SMs
+    if (in.split && force_split == 0 &&
+        (kind == dgk::kMasked ? (long long)num_groups * cdiv(m_rows, 128) : cdiv(m_rows, 128)) *
+                cdiv(n, in.block_n) >= num_sms)
+      continue;
     const int s_lo = in.split ? 2 : 1;
     // the heuristic splits no finer than one K group per CTA; a forced split
     // may (the CTAs without a K group add zeros)
@@ -132,14 +180,8 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
       else mblk = cdiv(m_rows, 128);
       const long long tiles = mblk * cdiv(n, in.block_n);
       const long long c = std::max(1, cap(i, in, S, smem));
-      const long long waves = cdiv(tiles, c);
-      const long long kper = cdiv(kb, S);
-      // Per wave: the K groups each CTA streams, weighted by the bytes of one
-      // K group (A: 128 rows, B: BN rows), plus a fixed cost per wave (first
-      // load latency, prologue, epilogue) worth about 12 K groups, plus the
-      // cluster reduction when the K groups are split.
-      const double unit = 128.0 + in.block_n;
-      double cost = (double)waves * (((double)kper + 12.0 + (S > 1 ? 4.0 : 0.0)) * unit);
+      const double t = est_time_us(in, S, tiles, c, num_sms, kind, m_rows, n, k, num_groups);
+      const double cost = t;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.inst = i;
@@ -152,7 +194,6 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
       }
     }
   }
-  (void)num_sms;
   return best;
 }
 
@@ -267,12 +308,12 @@ dg_status encode(CUtensorMap* m, CUtensorMapDataType dt, void* ptr, const uint64
 
 // A [z][rows][K] e4m3, B [g][N][K] e4m3, sa [z][kb][ld_sa] fp32, D [z][rows][N] bf16.
 dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, const void* B,
-                    void* D, int rows, int zA, int N, int K, int gB, int block_n) {
+                    void* D, int rows, int zA, int N, int K, int gB, int block_n, int a_rows) {
   const int kb = K / 128;
   {
     const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)zA};
     const uint64_t str[2] = {(uint64_t)K, (uint64_t)rows * K};
-    const uint32_t box[3] = {128, 128, 1};
+    const uint32_t box[3] = {128, (uint32_t)a_rows, 1};
     dg_status s = encode(&mp->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(A), dims, str,
                          box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
     if (s != DG_OK) return s;
@@ -373,7 +414,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
 
   dgk::Maps maps;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
-                kind == dgk::kDense ? 1 : G, in.block_n);
+                kind == dgk::kDense ? 1 : G, in.block_n, in.a_rows);
   if (s != DG_OK) return s;
 
   dgk::Params p{};

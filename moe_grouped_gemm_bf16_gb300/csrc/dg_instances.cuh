@@ -18,6 +18,7 @@ struct Instance {
   int stages;
   int split;  // 1: may run as a cluster with the K groups split across its CTAs
   int mode;
+  int a_rows;      // rows of A per tile loaded by TMA (128, or 64 for M <= 64)
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
                         cudaStream_t s);
@@ -37,9 +38,9 @@ const Instance* instances_masked(int* count);
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M>
 struct InstanceOf {
-  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE>;
+  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS>;
 
   static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
                             cudaStream_t s) {
@@ -48,13 +49,22 @@ struct InstanceOf {
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    // programmatic dependent launch: the prologue may overlap the previous
+    // kernel in the stream; the kernel waits for it before reading memory
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (SPLIT) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = cluster;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = SPLIT ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.sa, m.d, p);
   }
 
@@ -78,8 +88,9 @@ struct InstanceOf {
   }
 
   static Instance make() {
-    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, SmemLayout<BN, STAGES, SPLIT>::DYN_OFF + 1024,
-                    &launch, &set_smem, &max_clusters};
+    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS,
+                    SmemLayout<BN, STAGES, SPLIT, AROWS>::DYN_OFF + 1024, &launch, &set_smem,
+                    &max_clusters};
   }
 };
 

@@ -38,9 +38,12 @@
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT>
+// AROWS: rows of A loaded per tile (128, or 64 when M <= 64: the M=128 MMA
+// then reads rows 64..127 of its A operand from the neighbouring slot, in
+// bounds of the ring, and those output rows are discarded).
+template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M>
 struct SmemLayout {
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K;  // 16 KB e4m3
+  static constexpr int A_BYTES = AROWS * BLOCK_K;    // e4m3 A slot (16 KB or 8 KB)
   static constexpr int B_BYTES = BN * BLOCK_K;
   static constexpr int SA_BYTES = BLOCK_M * 4;       // 512 B fp32
   static constexpr int A_OFF = 0;
@@ -69,9 +72,9 @@ struct SmemLayout {
 };
 
 // Dynamic shared memory a launch needs (host side too).
-template <int BN, int STAGES, bool SPLIT>
+template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M>
 __host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
-  return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT>::DYN_OFF + 3 * kb * 4 +
+  return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS>::DYN_OFF + 3 * kb * 4 +
          (mode == kMasked ? (2 * num_groups + 1) * 4 : 0);
 }
 
@@ -181,17 +184,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
                 const Params p) {
   static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
-  using L = SmemLayout<BN, STAGES, SPLIT>;
+  static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
+  using L = SmemLayout<BN, STAGES, SPLIT, AROWS>;
   constexpr int HALF = BN / 2;                 // columns per promotion warpgroup
   constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup
-  constexpr int LDS_PER_WAIT = (HALF >= 128) ? 1 : 2;
   constexpr uint32_t IDESC = idesc_e4m3_f32(BLOCK_M, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -246,6 +249,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
     tmem_relinquish();
   }
+  // Everything above touched only shared memory, tensor memory and the kernel
+  // parameters; global memory (which the previous kernel in the stream may
+  // still be writing) is read only after this wait.  Dependent launches may
+  // start their own prologue from here on.
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   if (MODE == kMasked && warp == 2) {  // (warp 2 is otherwise idle)
     // valid rows per group (clamped to [0, max_m]) and the prefix sum of M blocks
     int carry = 0;
@@ -397,25 +406,28 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
           __syncwarp();
           tc_fence_after();
+          // warps whose TMEM lanes hold no loaded row of A have nothing to add
+          if (q * 32 < AROWS) {
           const float a_s = sa_ring[j * BLOCK_M + row];
           const float* sbg = sb_s + (g - kbeg);
+          const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
+          // 32-column chunks, software-pipelined: the load of chunk c+1 is in
+          // flight while chunk c is scaled and accumulated
+          uint32_t v[2][32];
+          tmem_ld_32x32b_x32(tcol, v[0]);
+          tmem_wait_ld(v[0]);
 #pragma unroll
-          for (int c0 = 0; c0 < NCH; c0 += LDS_PER_WAIT) {
-            uint32_t v[LDS_PER_WAIT][32];
+          for (int c = 0; c < NCH; ++c) {
+            if (c + 1 < NCH) tmem_ld_32x32b_x32(tcol + (c + 1) * 32, v[(c + 1) & 1]);
+            const int col = h * HALF + c * 32;
+            // the 32 columns lie in one 128-column B scale block
+            const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
 #pragma unroll
-            for (int u = 0; u < LDS_PER_WAIT; ++u)
-              tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * BN + h * HALF + (c0 + u) * 32),
-                                 v[u]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < LDS_PER_WAIT; ++u) {
-              const int col = h * HALF + (c0 + u) * 32;
-              // the 32 columns lie in one 128-column B scale block
-              const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                acc[(c0 + u) * 32 + i] = fmaf(__uint_as_float(v[u][i]), sc, acc[(c0 + u) * 32 + i]);
-            }
+            for (int i = 0; i < 32; i += 2)
+              ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], __uint_as_float(v[c & 1][i]),
+                    __uint_as_float(v[c & 1][i + 1]), sc);
+            if (c + 1 < NCH) tmem_wait_ld(v[(c + 1) & 1]);
+          }
           }
           tc_fence_before();
           __syncwarp();
@@ -510,10 +522,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         wait_bar<true>(bar(L::RED_FULL), k_iter & 1, abort_flag, p);
         __syncwarp();
-        // this CTA sums rows [r0, r1) of all S partials, in rank order
-        const int R = (BLOCK_M + S - 1) / S;
+        // this CTA sums rows [r0, r1) of the tile's valid rows, over all S
+        // partials, in rank order
+        const int R = (T.rows + S - 1) / S;
         const int r0 = static_cast<int>(crank) * R;
-        const int r1 = min(BLOCK_M, r0 + R);
+        const int r1 = min(T.rows, r0 + R);
         constexpr int UPR = BN / 4;
         for (int i = pt; i < max(0, r1 - r0) * UPR; i += 32 * NUM_PROMO_WARPS) {
           const int rr = r0 + i / UPR, cu = i % UPR;

@@ -163,6 +163,33 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.wait::ld that also names the 32 registers the preceding load fills,
+// so that the compiler cannot move any use of them above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+// {a0, a1} = {x0, x1} * {s, s} + {a0, a1}: one packed fp32x2 fused multiply-add
+// (round to nearest), the same arithmetic as two fmaf.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float x0, float x1, float s) {
+  asm("{\n\t.reg .b64 ra, rx, rs;\n\t"
+      "mov.b64 ra, {%0, %1};\n\t"
+      "mov.b64 rx, {%2, %3};\n\t"
+      "mov.b64 rs, {%4, %4};\n\t"
+      "fma.rn.f32x2 ra, rx, rs, ra;\n\t"
+      "mov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(s));
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i),
 // columns col .. col+31.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -241,6 +268,16 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
 // ------------------------------------------------------- named barriers ----
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (a no-op without the launch
+// attribute), and let the grids that depend on this one start their prologue.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Register reallocation between warpgroups (whole warpgroup executes it).
