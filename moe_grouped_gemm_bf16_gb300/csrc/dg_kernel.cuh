@@ -22,7 +22,7 @@
 //               deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
 //               Then the bf16 epilogue: a swizzled staging tile stored by TMA,
 //               or, when the K groups are split over a cluster, a fixed-order
-//               reduction of the partials through distributed shared memory.
+//               reduction of partials pushed through distributed shared memory.
 //
 // Every mbarrier wait is bounded: when one gives up it records a timeout in
 // the device status word and sets a CTA-wide abort flag, after which every
@@ -53,14 +53,14 @@ struct SmemLayout {
   // computes one tile, so after its last K group the operand ring is idle and
   // holds the fp32 partial of the reduction instead.
   static constexpr int OUT_OFF = SPLIT ? A_OFF : SA_OFF + SA_SLOTS * SA_BYTES;
-  static constexpr int OUT_BYTES = SPLIT ? BLOCK_M * BN * 4 : BLOCK_M * BN * 2;
-  static_assert(!SPLIT || OUT_BYTES <= STAGES * (A_BYTES + B_BYTES), "partial must fit the ring");
+  static constexpr int OUT_BYTES = SPLIT ? (BLOCK_M + MAX_SPLIT) * BN * 4 : BLOCK_M * BN * 2;
+  static_assert(!SPLIT || OUT_BYTES <= STAGES * (A_BYTES + B_BYTES), "partials must fit the ring");
   static constexpr int BAR_OFF = SPLIT ? SA_OFF + SA_SLOTS * SA_BYTES : OUT_OFF + OUT_BYTES;
   // barrier indexes
   static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
-                       T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, RED_EMPTY = RED_FULL + 1,
-                       MMA_DONE = RED_EMPTY + 1, NUM_BARS = MMA_DONE + 1;
+                       T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
+                       MMA_DONE = READY + 1, NUM_BARS = MMA_DONE + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int DYN_OFF = MISC_OFF + 16;            // sb tile, then masked tables
   static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
@@ -140,6 +140,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
     T.rows = min(BLOCK_M, mcnt[lo] - T.m0);
   }
   return T;
+}
+
+__device__ __forceinline__ int num_tiles_dense(const Params& p) {
+  return p.num_m_blocks * p.num_n_blocks;
 }
 
 // Bounded mbarrier wait.  Returns false (without waiting) once the CTA has
@@ -233,8 +237,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(bar(L::T_FULL + b), 1);
       mbar_init(bar(L::T_EMPTY + b), NUM_PROMO_WARPS);
     }
-    mbar_init(bar(L::RED_FULL), S);
-    mbar_init(bar(L::RED_EMPTY), S);
+    mbar_init(bar(L::RED_FULL), 1);
+    mbar_init(bar(L::READY), S);
     mbar_init(bar(L::MMA_DONE), 1);
     misc[1] = 0;
     fence_mbarrier_init();
@@ -249,10 +253,21 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
     tmem_relinquish();
   }
-  // Everything above touched only shared memory, tensor memory and the kernel
-  // parameters; global memory (which the previous kernel in the stream may
-  // still be writing) is read only after this wait.  Dependent launches may
-  // start their own prologue from here on.
+  if (MODE == kDense && warp == 0 && lane == 0 && !(p.debug_flags & DBG_SKIP_PRODUCER) &&
+      cluster_id < num_tiles_dense(p)) {
+    // Warm L2 with the first tiles' operands while an earlier kernel in the
+    // stream may still run.  A prefetch only fills L2, which stays coherent
+    // with any write that kernel still makes, so it is safe before the wait.
+    const Tile T = decode_tile<BN, MODE>(cluster_id, p, p.num_m_blocks, nullptr, nullptr);
+    for (int g = kbeg; g < min(kend, kbeg + STAGES); ++g) {
+      tma_prefetch_l2_3d(&tmA, g * BLOCK_K, T.m0, T.z);
+      tma_prefetch_l2_3d(&tmB, g * BLOCK_K, T.n0, T.e);
+    }
+  }
+  // Everything above touched only shared memory, tensor memory, the kernel
+  // parameters and L2 prefetches; global memory (which the previous kernel in
+  // the stream may still be writing) is read only after this wait.  Dependent
+  // launches may start their own prologue from here on.
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (MODE == kMasked && warp == 2) {  // (warp 2 is otherwise idle)
@@ -499,68 +514,66 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       } else {
-        // ------------- epilogue: K split over the cluster, DSMEM reduction --
-        // fp32 partial [128 rows][BN], 16-byte unit cu of row r stored at unit
-        // cu ^ (r & 7) (conflict-free row-per-thread writes, row-wise reads)
-        wait_bar<true>(bar(L::RED_EMPTY), (k_iter & 1) ^ 1, abort_flag, p);
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int cu = (h * HALF + c * 32) / 4 + u;
-            const int o = c * 32 + u * 4;
-            st_shared_v4(out_s + row * (BN * 4) + ((cu ^ (row & 7)) << 4), __float_as_uint(acc[o]),
-                         __float_as_uint(acc[o + 1]), __float_as_uint(acc[o + 2]),
-                         __float_as_uint(acc[o + 3]));
-          }
-        }
-        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
-        if (pt == 0) {
-          fence_acq_rel_cluster();
-          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::RED_FULL), r);
-        }
-        wait_bar<true>(bar(L::RED_FULL), k_iter & 1, abort_flag, p);
-        __syncwarp();
-        // this CTA sums rows [r0, r1) of the tile's valid rows, over all S
-        // partials, in rank order
+        // ------------- epilogue: K split over the cluster, push reduction ---
+        // Each CTA owns a slice of R = ceil(rows / S) tile rows.  Every thread
+        // pushes its row's fp32 partial with st.async into the owner's receive
+        // buffer (slot [sender rank][row in slice][column], in the owner's
+        // operand ring, idle by now), completing bytes on the owner's RED_FULL
+        // barrier; the owner then sums the S partials in rank order and stores
+        // bf16.  READY (S arrivals) tells every CTA that all rings are idle.
         const int R = (T.rows + S - 1) / S;
-        const int r0 = static_cast<int>(crank) * R;
-        const int r1 = min(T.rows, r0 + R);
-        constexpr int UPR = BN / 4;
-        for (int i = pt; i < max(0, r1 - r0) * UPR; i += 32 * NUM_PROMO_WARPS) {
-          const int rr = r0 + i / UPR, cu = i % UPR;
-          const int m = T.m0 + rr, n = T.n0 + cu * 4;
-          if (m < p.M && n < p.N) {
-            const uint32_t off = out_s + rr * (BN * 4) + ((cu ^ (rr & 7)) << 4);
-            // issue every rank's load first, then add in rank order
-            float4 v[MAX_SPLIT];
+        const int own_r0 = static_cast<int>(crank) * R;
+        const int own_rows = max(0, min(T.rows, own_r0 + R) - own_r0);
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);  // this CTA's ring is idle
+        if (pt == 0) {
+          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>(S * own_rows * BN * 4));
+          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::READY), r);
+        }
+        wait_bar<true>(bar(L::READY), 0, abort_flag, p);
+        __syncwarp();
+        if (row < T.rows) {
+          const int owner = row / R;
+          const uint32_t dst = map_cluster(
+              out_s + static_cast<uint32_t>(((static_cast<int>(crank) * R + (row - owner * R)) * BN +
+                                             h * HALF) * 4),
+              owner);
+          const uint32_t rbar = map_cluster(bar(L::RED_FULL), owner);
 #pragma unroll
-            for (int r = 0; r < MAX_SPLIT; ++r)
-              if (r < S) v[r] = ld_cluster_f4(map_cluster(off, r));
-            float4 sum = v[0];
+          for (int c = 0; c < HALF / 4; ++c)
+            st_async_v4(dst + c * 16, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3],
+                        rbar);
+        }
+        wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
+        __syncwarp();
+        constexpr int UPR = BN / 4;  // 16-byte units per row
+        for (int i = pt; i < own_rows * UPR; i += 32 * NUM_PROMO_WARPS) {
+          const int rr = i / UPR, cu = i - rr * UPR;
+          const int n = T.n0 + cu * 4;
+          float4 v[MAX_SPLIT];
 #pragma unroll
-            for (int r = 1; r < MAX_SPLIT; ++r)
-              if (r < S) {
-                sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
-              }
-            if (!*abort_flag) {
-              uint2 w;
-              w.x = pack_bf16x2(sum.x, sum.y);
-              w.y = pack_bf16x2(sum.z, sum.w);
-              *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(m) * p.N + n) = w;
+          for (int r = 0; r < MAX_SPLIT; ++r)
+            if (r < S) {
+              const uint4 w = ld_shared_v4(out_s + static_cast<uint32_t>(((r * R + rr) * BN + cu * 4) * 4));
+              v[r] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                 __uint_as_float(w.w));
             }
+          float4 sum = v[0];
+#pragma unroll
+          for (int r = 1; r < MAX_SPLIT; ++r)
+            if (r < S) {
+              sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
+            }
+          if (n < p.N && !*abort_flag) {
+            uint2 w;
+            w.x = pack_bf16x2(sum.x, sum.y);
+            w.y = pack_bf16x2(sum.z, sum.w);
+            *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(T.m0 + own_r0 + rr) * p.N + n) = w;
           }
         }
-        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
-        if (pt == 0)
-          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::RED_EMPTY), r);
+        // every byte pushed to this CTA has landed before it may exit
+        if (pt == 0) drain_wait(bar(L::RED_FULL), 0, p);
       }
     }  // tile loop
-    if (SPLIT && k_iter > 0) {
-      // the other CTAs must be done reading this CTA's last partial
-      wait_bar<true>(bar(L::RED_EMPTY), (k_iter & 1) ^ 1, abort_flag, p);
-    }
     if (pt == 0) bulk_wait_group0();
     __syncwarp();
   }
