@@ -9,7 +9,6 @@ const Instance* instances_dense(int* count) {
       InstanceOf<256, 3, false, kDense>::make(),
       InstanceOf<128, 6, true, kDense>::make(),
       InstanceOf<128, 8, true, kDense, 64>::make(),
-      InstanceOf<256, 4, true, kDense>::make(),
       InstanceOf<256, 5, true, kDense, 64>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));

@@ -53,7 +53,8 @@ struct SmemLayout {
   // computes one tile, so after its last K group the operand ring is idle and
   // holds the fp32 partial of the reduction instead.
   static constexpr int OUT_OFF = SPLIT ? A_OFF : SA_OFF + SA_SLOTS * SA_BYTES;
-  static constexpr int OUT_BYTES = SPLIT ? (BLOCK_M + MAX_SPLIT) * BN * 4 : BLOCK_M * BN * 2;
+  // split: own partial [128][BN] fp32 + received slices [S][ceil(rows/S)][BN] fp32
+  static constexpr int OUT_BYTES = SPLIT ? (2 * AROWS + MAX_SPLIT) * BN * 4 : BLOCK_M * BN * 2;
   static_assert(!SPLIT || OUT_BYTES <= STAGES * (A_BYTES + B_BYTES), "partials must fit the ring");
   static constexpr int BAR_OFF = SPLIT ? SA_OFF + SA_SLOTS * SA_BYTES : OUT_OFF + OUT_BYTES;
   // barrier indexes
@@ -253,21 +254,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
     tmem_relinquish();
   }
-  if (MODE == kDense && warp == 0 && lane == 0 && !(p.debug_flags & DBG_SKIP_PRODUCER) &&
-      cluster_id < num_tiles_dense(p)) {
-    // Warm L2 with the first tiles' operands while an earlier kernel in the
-    // stream may still run.  A prefetch only fills L2, which stays coherent
-    // with any write that kernel still makes, so it is safe before the wait.
-    const Tile T = decode_tile<BN, MODE>(cluster_id, p, p.num_m_blocks, nullptr, nullptr);
-    for (int g = kbeg; g < min(kend, kbeg + STAGES); ++g) {
-      tma_prefetch_l2_3d(&tmA, g * BLOCK_K, T.m0, T.z);
-      tma_prefetch_l2_3d(&tmB, g * BLOCK_K, T.n0, T.e);
-    }
-  }
-  // Everything above touched only shared memory, tensor memory, the kernel
-  // parameters and L2 prefetches; global memory (which the previous kernel in
-  // the stream may still be writing) is read only after this wait.  Dependent
-  // launches may start their own prologue from here on.
+  // Everything above touched only shared memory, tensor memory and the kernel
+  // parameters; global memory (which the previous kernel in the stream may
+  // still be writing) is read only after this wait.  Dependent launches may
+  // start their own prologue from here on.
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (MODE == kMasked && warp == 2) {  // (warp 2 is otherwise idle)
@@ -514,46 +504,60 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
       } else {
-        // ------------- epilogue: K split over the cluster, push reduction ---
-        // Each CTA owns a slice of R = ceil(rows / S) tile rows.  Every thread
-        // pushes its row's fp32 partial with st.async into the owner's receive
-        // buffer (slot [sender rank][row in slice][column], in the owner's
-        // operand ring, idle by now), completing bytes on the owner's RED_FULL
-        // barrier; the owner then sums the S partials in rank order and stores
-        // bf16.  READY (S arrivals) tells every CTA that all rings are idle.
+        // ------------- epilogue: K split over the cluster, DSMEM reduction ---
+        // Each CTA owns a slice of R = ceil(rows / S) tile rows.  A CTA stages
+        // its fp32 partial rows in its (now idle) operand ring, 16-byte unit u
+        // of row r at unit u ^ (r & 7) (conflict-free row-per-thread writes),
+        // then one thread sends each owner its slice with a bulk copy into the
+        // owner's receive area (slot [sender rank][row in slice]), completing
+        // bytes on the owner's RED_FULL.  The owner sums the S slices in rank
+        // order and stores bf16.  READY (S arrivals) tells every CTA that all
+        // rings are idle, so receive areas may be written.
         const int R = (T.rows + S - 1) / S;
         const int own_r0 = static_cast<int>(crank) * R;
         const int own_rows = max(0, min(T.rows, own_r0 + R) - own_r0);
-        named_bar_sync(1, 32 * NUM_PROMO_WARPS);  // this CTA's ring is idle
+        constexpr int ROWB = BN * 4;                       // bytes of one fp32 row
+        const uint32_t stage_s = out_s;                    // [rows <= AROWS][BN] own partial
+        const uint32_t recv_s = out_s + AROWS * ROWB;      // [S][R][BN] received slices
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);           // this CTA's ring is idle
+        if (row < T.rows) {
+#pragma unroll
+          for (int c = 0; c < HALF / 4; ++c) {
+            const int u = h * (HALF / 4) + c;
+            st_shared_v4(stage_s + row * ROWB + ((u ^ (row & 7)) << 4), __float_as_uint(acc[4 * c]),
+                         __float_as_uint(acc[4 * c + 1]), __float_as_uint(acc[4 * c + 2]),
+                         __float_as_uint(acc[4 * c + 3]));
+          }
+        }
+        fence_proxy_async_smem();  // the bulk copies read what this thread wrote
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         if (pt == 0) {
-          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>(S * own_rows * BN * 4));
+          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>(S * own_rows * ROWB));
           for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::READY), r);
         }
         wait_bar<true>(bar(L::READY), 0, abort_flag, p);
         __syncwarp();
-        if (row < T.rows) {
-          const int owner = row / R;
-          const uint32_t dst = map_cluster(
-              out_s + static_cast<uint32_t>(((static_cast<int>(crank) * R + (row - owner * R)) * BN +
-                                             h * HALF) * 4),
-              owner);
-          const uint32_t rbar = map_cluster(bar(L::RED_FULL), owner);
-#pragma unroll
-          for (int c = 0; c < HALF / 4; ++c)
-            st_async_v4(dst + c * 16, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3],
-                        rbar);
+        if (pt == 0) {
+          for (int o = 0; o < S; ++o) {
+            const int rows_o = max(0, min(T.rows, (o + 1) * R) - o * R);
+            if (rows_o == 0) continue;
+            bulk_copy_to_cluster(map_cluster(recv_s + static_cast<uint32_t>(crank) * R * ROWB, o),
+                                 stage_s + o * R * ROWB, static_cast<uint32_t>(rows_o * ROWB),
+                                 map_cluster(bar(L::RED_FULL), o));
+          }
         }
         wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
         __syncwarp();
         constexpr int UPR = BN / 4;  // 16-byte units per row
         for (int i = pt; i < own_rows * UPR; i += 32 * NUM_PROMO_WARPS) {
           const int rr = i / UPR, cu = i - rr * UPR;
-          const int n = T.n0 + cu * 4;
+          const int grow = own_r0 + rr;  // row in the tile (its swizzle key)
+          const uint32_t off = static_cast<uint32_t>(rr * ROWB + ((cu ^ (grow & 7)) << 4));
           float4 v[MAX_SPLIT];
 #pragma unroll
           for (int r = 0; r < MAX_SPLIT; ++r)
             if (r < S) {
-              const uint4 w = ld_shared_v4(out_s + static_cast<uint32_t>(((r * R + rr) * BN + cu * 4) * 4));
+              const uint4 w = ld_shared_v4(recv_s + static_cast<uint32_t>(r * R * ROWB) + off);
               v[r] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                                  __uint_as_float(w.w));
             }
@@ -563,14 +567,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (r < S) {
               sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
             }
+          const int n = T.n0 + cu * 4;
           if (n < p.N && !*abort_flag) {
             uint2 w;
             w.x = pack_bf16x2(sum.x, sum.y);
             w.y = pack_bf16x2(sum.z, sum.w);
-            *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(T.m0 + own_r0 + rr) * p.N + n) = w;
+            *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(T.m0 + grow) * p.N + n) = w;
           }
         }
-        // every byte pushed to this CTA has landed before it may exit
+        // every byte sent to this CTA has landed before it may exit
         if (pt == 0) drain_wait(bar(L::RED_FULL), 0, p);
       }
     }  // tile loop

@@ -275,6 +275,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
       : "memory");
 }
 
+// Bulk copy from this CTA's shared memory into another CTA's (addresses from
+// mapa), counted in bytes on that CTA's mbarrier.  Addresses and size: 16-byte
+// multiples.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
 // Prefetch one TMA box into L2 (no shared memory, no completion to track).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(

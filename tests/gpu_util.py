@@ -88,7 +88,9 @@ def run_masked(p, expected_m=None, fill=W.BF16_SENTINEL, masked_m=None):
 
 
 class forced_config:
-    """Context manager: force (block_n, split_k) for the launches inside."""
+    """Context manager: force (block_n, split_k) for the launches inside.  A
+    configuration the library has no kernel for (for example a K split with
+    256-wide tiles and more than 64 rows) skips the test."""
 
     def __init__(self, block_n, split_k):
         self.cfg = (block_n, split_k)
@@ -96,5 +98,8 @@ class forced_config:
     def __enter__(self):
         dg.debug_force_config(*self.cfg)
 
-    def __exit__(self, *a):
+    def __exit__(self, exc_type, exc, tb):
         dg.debug_force_config(0, 0)
+        if exc_type is dg.DGError and exc.status == 2 and self.cfg != (0, 0):
+            import pytest
+            pytest.skip(f"no kernel for forced config {self.cfg}")
