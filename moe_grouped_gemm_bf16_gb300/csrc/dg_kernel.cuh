@@ -533,7 +533,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         if (pt == 0) {
           mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>(S * own_rows * ROWB));
-          for (int r = 0; r < S; ++r) mbar_arrive_remote(bar(L::READY), r);
+          // a signal only: the ring's idleness was already observed through
+          // the mbarriers of its last loads and MMAs
+          for (int r = 0; r < S; ++r) mbar_arrive_remote_relaxed(bar(L::READY), r);
         }
         wait_bar<true>(bar(L::READY), 0, abort_flag, p);
         __syncwarp();
@@ -590,7 +592,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
-  if (SPLIT) cluster_sync();
+  // no CTA leaves while a peer may still copy into it; every exchanged byte
+  // has been consumed by now, so the rendezvous needs no memory ordering
+  if (SPLIT) cluster_sync_relaxed();
 }
 
 }  // namespace dgk
