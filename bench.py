@@ -130,15 +130,20 @@ def kernel_source_hash():
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/<workload>_traffic.txt), if it was taken on the current kernel
+    sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_traffic.txt")
     try:
+        kv = {}
         with open(path) as fh:
-            d = json.load(fh)
-        e = d.get(workload)
-        if e and e.get("kernel_hash") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            for line in fh:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_hash") == kernel_source_hash():
+            return float(kv["dram_bytes_per_launch"])
     except Exception:
         pass
     return None
