@@ -125,13 +125,14 @@ dg_status dg_get_device_status(void* stream);
  * needed).  kind: 0 dense, 1 contiguous, 2 masked.  m is M (dense), M_total
  * (contiguous) or expected_m (masked).  num_sms is the SM count to plan for. */
 typedef struct dg_config {
-  int block_m;      /* 128 */
+  int block_m;      /* output tile height: 128, or 256 in the CTA-pair form */
   int block_n;      /* output tile width */
   int split_k;      /* CTAs per cluster sharing one tile's K groups (dense only) */
   int stages;       /* depth of the shared-memory ring */
   int num_tiles;    /* output tiles (masked: from expected_m) */
   int grid;         /* CTAs launched */
   int smem_bytes;   /* dynamic shared memory per CTA */
+  int pair;         /* 1: CTA-pair form (a 2-CTA cluster computes each block_m = 256 tile) */
 } dg_config;
 dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
                          dg_config* out);
@@ -157,6 +158,12 @@ dg_status dg_debug_set_skip_producer(int on);
  * return DG_ERR_UNSUPPORTED_SHAPE.  The environment variable
  * DG_FORCE_CONFIG="block_n,split_k" sets the same at start-up. */
 dg_status dg_debug_force_config(int block_n, int split_k);
+
+/* Test and benchmark hook: -1 (default) lets the heuristic decide whether a
+ * dense GEMM runs in the CTA-pair form (256-row tiles computed by a 2-CTA
+ * cluster with one shared MMA); 0 never, 1 always (dense only; the grouped
+ * forms have no pair kernel, so 1 makes them return DG_ERR_UNSUPPORTED_SHAPE). */
+dg_status dg_debug_force_pair(int mode);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,7 @@ __all__ = [
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
     "plan_config", "num_output_tiles", "set_wait_timeout_ns", "debug_set_skip_producer",
-    "debug_force_config", "STATUS_NAMES", "EXPORTED_SYMBOLS",
+    "debug_force_config", "debug_force_pair", "STATUS_NAMES", "EXPORTED_SYMBOLS",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = [
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_num_output_tiles",
     "dg_set_wait_timeout_ns", "dg_debug_set_skip_producer", "dg_debug_force_config",
+    "dg_debug_force_pair",
 ]
 
 
@@ -48,7 +49,8 @@ class DGError(RuntimeError):
 
 class DGConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("block_m", "block_n", "split_k", "stages", "num_tiles", "grid", "smem_bytes")]
+                ("block_m", "block_n", "split_k", "stages", "num_tiles", "grid", "smem_bytes",
+                 "pair")]
 
 
 _LIB = None
@@ -82,6 +84,7 @@ def lib():
         L.dg_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
         L.dg_debug_set_skip_producer.argtypes = [_i]
         L.dg_debug_force_config.argtypes = [_i, _i]
+        L.dg_debug_force_pair.argtypes = [_i]
         for f in EXPORTED_SYMBOLS:
             if f not in ("dg_last_error_string", "dg_num_output_tiles"):
                 getattr(L, f).restype = _i
@@ -178,3 +181,7 @@ def debug_set_skip_producer(on):
 
 def debug_force_config(block_n=0, split_k=0):
     _check(lib().dg_debug_force_config(int(block_n), int(split_k)))
+
+
+def debug_force_pair(mode=-1):
+    _check(lib().dg_debug_force_pair(int(mode)))

@@ -49,6 +49,7 @@ std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_skip_producer{0};
 std::atomic<int> g_force_bn{-1};     // -1: not read from the environment yet; 0: auto
 std::atomic<int> g_force_split{0};
+std::atomic<int> g_force_pair{-1};   // -1: heuristic; 0: no pair form; 1: pair form only
 
 constexpr int kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class GPUs
 constexpr int kMaxDevices = 64;
@@ -99,6 +100,7 @@ long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 struct Plan {
   int inst = -1;
   int split = 1;
+  int pair = 0;
   long long tiles = 0;
   int clusters = 0;
   int smem = 0;
@@ -111,7 +113,12 @@ struct Plan {
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
   const double ghz = 2.0;
-  const double t_mma = (in.block_n <= 128 ? 454.0 : 643.0 * in.block_n / 256.0) / (ghz * 1e3);
+  double t_mma = (in.block_n <= 128 ? 454.0 : 643.0 * in.block_n / 256.0) / (ghz * 1e3);
+  // operand delivery: each K group brings (A rows + B rows this CTA loads) x 128
+  // bytes at ~120 GB/s per SM, and shares shared-memory bandwidth with the MMA
+  const double b_rows = in.pair ? in.block_n / 2.0 : (double)in.block_n;
+  const double t_in = (in.a_rows + b_rows) * 128.0 / 120e3;
+  t_mma = std::max(t_mma, t_in);
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
   long long ctas, rounds;
@@ -119,6 +126,11 @@ double est_time_us(const Instance& in, int S, long long tiles, long long cluster
     // one cluster per tile, as many waves as the resident clusters need
     rounds = cdiv(tiles, clusters_resident);
     ctas = std::min<long long>(tiles, clusters_resident) * S;
+  } else if (in.pair) {
+    // tiles are 256 rows, one per CTA pair
+    const long long pairs = std::max<long long>(1, std::min<long long>(tiles, clusters_resident));
+    ctas = 2 * pairs;
+    rounds = cdiv(tiles, pairs);
   } else {
     ctas = std::min<long long>(tiles, num_sms);
     rounds = cdiv(tiles, ctas);  // tiles one persistent CTA computes in turn
@@ -157,6 +169,11 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     if (force_bn > 0 && in.block_n != force_bn) continue;
     // 64-row A tiles serve M <= 64 only, and are the choice there
     if (in.a_rows < 128 && m_rows > in.a_rows) continue;
+    // 256-row pair tiles only pay off with more than one 128-row block
+    const int fp = g_force_pair.load();
+    if (fp == 0 && in.pair) continue;
+    if (fp == 1 && !in.pair) continue;
+    if (fp < 0 && in.pair && m_rows <= 128) continue;
     if (in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;
@@ -177,9 +194,9 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
       }
       long long mblk;
       if (kind == dgk::kMasked) mblk = (long long)num_groups * cdiv(m_rows, 128);
-      else mblk = cdiv(m_rows, 128);
+      else mblk = cdiv(m_rows, in.pair ? 256 : 128);
       const long long tiles = mblk * cdiv(n, in.block_n);
-      const long long c = std::max(1, cap(i, in, S, smem));
+      const long long c = std::max(1, cap(i, in, in.pair ? 2 : S, smem));
       const double t = est_time_us(in, S, tiles, c, num_sms, kind, m_rows, n, k, num_groups);
       const double cost = t;
       if (cost < best_cost - 1e-9) {
@@ -190,6 +207,7 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
         // the split form runs one cluster per tile (its epilogue reuses the
         // operand ring); the others are persistent, at most one wave of CTAs
         best.clusters = in.split ? (int)tiles : (int)std::min<long long>(tiles, c);
+        best.pair = in.pair;
         best.smem = smem;
       }
     }
@@ -410,11 +428,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
     const long long ub = (long long)G * cdiv(rows, 128) * cdiv(N, in.block_n);
     clusters = (int)std::min<long long>(ub, num_sms);
   }
-  const int grid = std::max(1, clusters) * pl.split;
+  const int grid = std::max(1, clusters) * (in.pair ? 2 : pl.split);
 
   dgk::Maps maps;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
-                kind == dgk::kDense ? 1 : G, in.block_n, in.a_rows);
+                kind == dgk::kDense ? 1 : G, in.pair ? in.block_n / 2 : in.block_n, in.a_rows);
   if (s != DG_OK) return s;
 
   dgk::Params p{};
@@ -424,7 +442,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.kb = K / 128;
   p.nb = (N + 127) / 128;
   p.num_groups = kind == dgk::kDense ? 1 : G;
-  p.num_m_blocks = (int)cdiv(rows, 128);
+  p.num_m_blocks = (int)cdiv(rows, in.pair ? 256 : 128);
   p.num_n_blocks = (int)cdiv(N, in.block_n);
   p.raster_m = kRasterM;
   p.split_k = pl.split;
@@ -436,7 +454,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.timeout_ns = g_timeout_ns.load();
   p.debug_flags = g_skip_producer.load() ? dgk::DBG_SKIP_PRODUCER : 0u;
 
-  const cudaError_t e = in.launch(maps, p, grid, pl.split, pl.smem,
+  const cudaError_t e = in.launch(maps, p, grid, in.pair ? 2 : pl.split, pl.smem,
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -549,12 +567,13 @@ dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_
   const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load());
   if (pl.inst < 0) return fail(DG_ERR_UNSUPPORTED_SHAPE, "no configuration");
   const Instance& in = table_for(kind).p[pl.inst];
-  out->block_m = dgk::BLOCK_M;
+  out->block_m = in.pair ? 2 * dgk::BLOCK_M : dgk::BLOCK_M;
+  out->pair = in.pair;
   out->block_n = in.block_n;
   out->split_k = pl.split;
   out->stages = in.stages;
   out->num_tiles = (int)pl.tiles;
-  out->grid = std::max(1, pl.clusters) * pl.split;
+  out->grid = std::max(1, pl.clusters) * (pl.pair ? 2 : pl.split);
   out->smem_bytes = pl.smem;
   return ok();
 }
@@ -571,6 +590,12 @@ dg_status dg_set_wait_timeout_ns(unsigned long long ns) {
 
 dg_status dg_debug_set_skip_producer(int on) {
   g_skip_producer.store(on ? 1 : 0);
+  return ok();
+}
+
+dg_status dg_debug_force_pair(int mode) {
+  if (mode < -1 || mode > 1) return fail(DG_ERR_INVALID_ARG, "pair mode %d", mode);
+  g_force_pair.store(mode);
   return ok();
 }
 

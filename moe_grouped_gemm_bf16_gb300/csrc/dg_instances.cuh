@@ -19,6 +19,7 @@ struct Instance {
   int split;  // 1: may run as a cluster with the K groups split across its CTAs
   int mode;
   int a_rows;      // rows of A per tile loaded by TMA (128, or 64 for M <= 64)
+  int pair;        // 1: CTA-pair form (cta_group::2, 256-row tiles over a 2-CTA cluster)
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
                         cudaStream_t s);
@@ -38,9 +39,9 @@ const Instance* instances_masked(int* count);
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false>
 struct InstanceOf {
-  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS>;
+  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS, PAIR>;
 
   static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
                             cudaStream_t s) {
@@ -56,7 +57,7 @@ struct InstanceOf {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
-    if (SPLIT) {
+    if (SPLIT || PAIR) {
       attr[n].id = cudaLaunchAttributeClusterDimension;
       attr[n].val.clusterDim.x = cluster;
       attr[n].val.clusterDim.y = 1;
@@ -88,9 +89,9 @@ struct InstanceOf {
   }
 
   static Instance make() {
-    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS,
-                    SmemLayout<BN, STAGES, SPLIT, AROWS>::DYN_OFF + 1024, &launch, &set_smem,
-                    &max_clusters};
+    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0,
+                    SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF + 1024, &launch,
+                    &set_smem, &max_clusters};
   }
 };
 

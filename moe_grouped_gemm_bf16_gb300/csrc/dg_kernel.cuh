@@ -41,10 +41,11 @@ namespace dgk {
 // AROWS: rows of A loaded per tile (128, or 64 when M <= 64: the M=128 MMA
 // then reads rows 64..127 of its A operand from the neighbouring slot, in
 // bounds of the ring, and those output rows are discarded).
-template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M>
+// PAIR: the CTA pair form (cta_group::2): each CTA holds half of the B tile.
+template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false>
 struct SmemLayout {
   static constexpr int A_BYTES = AROWS * BLOCK_K;    // e4m3 A slot (16 KB or 8 KB)
-  static constexpr int B_BYTES = BN * BLOCK_K;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BLOCK_K;
   static constexpr int SA_BYTES = BLOCK_M * 4;       // 512 B fp32
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
@@ -73,9 +74,10 @@ struct SmemLayout {
 };
 
 // Dynamic shared memory a launch needs (host side too).
-template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M>
+template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false>
 __host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
-  return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS>::DYN_OFF + 3 * kb * 4 +
+  return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF +
+         3 * kb * 4 +
          (mode == kMasked ? (2 * num_groups + 1) * 4 : 0);
 }
 
@@ -97,9 +99,12 @@ __device__ __forceinline__ void raise_status(const Params& p, unsigned int code)
 // blocks and then across N, so the tiles running at the same time share A
 // rows and B columns in L2 (block scheduler with rasterisation, DeepGEMM
 // overview deepep.org/zh/deepgemm, "统一优化的块调度器").
-template <int BN, int MODE>
+// In the pair form an M block is 256 rows, of which CTA `crank` of the pair
+// owns rows [128 * crank, 128 * crank + 128).
+template <int BN, int MODE, bool PAIR = false>
 __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_blocks,
-                                            const int* prefix, const int* mcnt) {
+                                            const int* prefix, const int* mcnt,
+                                            uint32_t crank = 0) {
   const int nN = p.num_n_blocks;
   const int band_tiles = p.raster_m * nN;
   const int band = t / band_tiles;
@@ -111,10 +116,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
   T.n0 = (r / bh) * BN;
   T.skip = 0;
   if (MODE == kDense) {
-    T.m0 = mb * BLOCK_M;
+    T.m0 = PAIR ? mb * 2 * BLOCK_M + static_cast<int>(crank) * BLOCK_M : mb * BLOCK_M;
     T.z = 0;
     T.e = 0;
-    T.rows = min(BLOCK_M, p.M - T.m0);
+    T.rows = max(0, min(BLOCK_M, p.M - T.m0));
   } else if (MODE == kContiguous) {
     T.m0 = mb * BLOCK_M;
     T.z = 0;
@@ -189,7 +194,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
@@ -197,10 +202,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
-  using L = SmemLayout<BN, STAGES, SPLIT, AROWS>;
+  static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && BN == 256),
+                "the pair form: dense, full A, 256-wide tiles");
+  using L = SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>;
   constexpr int HALF = BN / 2;                 // columns per promotion warpgroup
   constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup
-  constexpr uint32_t IDESC = idesc_e4m3_f32(BLOCK_M, BN);
+  // the pair MMA spans both CTAs' 128 rows
+  constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BLOCK_M : BLOCK_M, BN);
 
   extern __shared__ uint8_t smem_raw[];
   // swizzled tiles need 1024-byte aligned shared-memory addresses
@@ -216,10 +224,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   int* mcnt = prefix + p.num_groups + 1;
   const float* sa_ring = reinterpret_cast<const float*>(smem + L::SA_OFF);
 
-  const uint32_t crank = SPLIT ? cluster_ctarank() : 0;
-  const int S = SPLIT ? p.split_k : 1;
-  const int cluster_id = blockIdx.x / S;
-  const int num_clusters = gridDim.x / S;
+  const uint32_t crank = (SPLIT || PAIR) ? cluster_ctarank() : 0;
+  const int S = SPLIT ? p.split_k : 1;           // CTAs sharing one tile's K groups
+  const int CL = PAIR ? 2 : S;                   // CTAs per cluster
+  const bool leader = crank == 0;                // pair form: the CTA that issues the MMAs
+  const int cluster_id = blockIdx.x / CL;
+  const int num_clusters = gridDim.x / CL;
   const int kbeg = static_cast<int>(static_cast<long long>(crank) * p.kb / S);
   const int kend = static_cast<int>(static_cast<long long>(crank + 1) * p.kb / S);
   const int kcnt = kend - kbeg;
@@ -236,7 +246,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     for (int b = 0; b < L::NBUF; ++b) {
       mbar_init(bar(L::T_FULL + b), 1);
-      mbar_init(bar(L::T_EMPTY + b), NUM_PROMO_WARPS);
+      // pair form: the leader's barrier counts both CTAs' promotion warps
+      mbar_init(bar(L::T_EMPTY + b), PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
     }
     mbar_init(bar(L::RED_FULL), 1);
     mbar_init(bar(L::READY), S);
@@ -251,8 +262,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     prefetch_tmap(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(sbase + L::MISC_OFF, L::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   // Everything above touched only shared memory, tensor memory and the kernel
   // parameters; global memory (which the previous kernel in the stream may
@@ -287,7 +303,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (SPLIT) cluster_sync();
+  if (SPLIT || PAIR) cluster_sync();
   const uint32_t tmem_base = misc[0];
   const int num_m_blocks = (MODE == kMasked) ? prefix[p.num_groups] : p.num_m_blocks;
   const int num_tiles = num_m_blocks * p.num_n_blocks;
@@ -310,15 +326,26 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int s = 0, j = 0;
       uint32_t ph = 0, jph = 0;
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
-        const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
         if (T.skip) continue;
         for (int g = kbeg; g < kend; ++g) {
           if (wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p)) {
-            mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + L::B_BYTES);
-            tma_load_3d(sbase + L::A_OFF + s * L::A_BYTES, &tmA, bar(L::FULL + s), g * BLOCK_K,
-                        T.m0, T.z);
-            tma_load_3d(sbase + L::B_OFF + s * L::B_BYTES, &tmB, bar(L::FULL + s), g * BLOCK_K,
-                        T.n0, T.e);
+            if constexpr (PAIR) {
+              // both CTAs' loads complete on the leader's FULL barrier, which
+              // expects the bytes of both
+              const uint32_t full = map_cluster(bar(L::FULL + s), 0);
+              if (leader) mbar_arrive_expect_tx(bar(L::FULL + s), 2 * (L::A_BYTES + L::B_BYTES));
+              tma_load_3d_pair(sbase + L::A_OFF + s * L::A_BYTES, &tmA, full, g * BLOCK_K, T.m0,
+                               T.z);
+              tma_load_3d_pair(sbase + L::B_OFF + s * L::B_BYTES, &tmB, full, g * BLOCK_K,
+                               T.n0 + static_cast<int>(crank) * (BN / 2), T.e);
+            } else {
+              mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + L::B_BYTES);
+              tma_load_3d(sbase + L::A_OFF + s * L::A_BYTES, &tmA, bar(L::FULL + s), g * BLOCK_K,
+                          T.m0, T.z);
+              tma_load_3d(sbase + L::B_OFF + s * L::B_BYTES, &tmB, bar(L::FULL + s), g * BLOCK_K,
+                          T.n0, T.e);
+            }
             issued_mask |= 1u << s;
             issued_par = (issued_par & ~(1u << s)) | (ph << s);
           }
@@ -336,19 +363,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       // Drain: after an abort the latest load into a slot may still be in
       // flight; wait for it before the CTA can exit.  (After a normal run every
       // load has been consumed already and these waits return at once.)
+      // (pair form: the leader's FULL barriers count both CTAs' loads, and the
+      // leader drains them; the CTAs leave only together, after a rendezvous)
       for (int q = 0; q < STAGES; ++q)
-        if ((issued_mask >> q) & 1u) drain_wait(bar(L::FULL + q), (issued_par >> q) & 1u, p);
+        if (((issued_mask >> q) & 1u) && (!PAIR || leader))
+          drain_wait(bar(L::FULL + q), (issued_par >> q) & 1u, p);
       for (int q = 0; q < SA_SLOTS; ++q)
         if ((sa_issued_mask >> q) & 1u) drain_wait(bar(L::SA_FULL + q), (sa_issued_par >> q) & 1u, p);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer ---
-    if (lane == 0) {
+    // (pair form: the leader issues for both CTAs; the other CTA's warp 1 only
+    // takes part in the collective TMEM allocation)
+    if (lane == 0 && (!PAIR || leader)) {
       int s = 0, b = 0;
       uint32_t ph = 0, bph = 0;
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
-        const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
         if (T.skip) continue;
         for (int g = kbeg; g < kend; ++g) {
           const bool ok_t = wait_bar(bar(L::T_EMPTY + b), bph ^ 1, abort_flag, p);
@@ -359,18 +391,28 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
             const uint64_t ad = smem_desc_sw128_kmajor(sbase + L::A_OFF + s * L::A_BYTES);
             const uint64_t bd = smem_desc_sw128_kmajor(sbase + L::B_OFF + s * L::B_BYTES);
+            if constexpr (PAIR) {
 #pragma unroll
-            for (int kk = 0; kk < BLOCK_K / 32; ++kk)
-              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
-            mma_commit(bar(L::EMPTY + s));
-            mma_commit(bar(L::T_FULL + b));
+              for (int kk = 0; kk < BLOCK_K / 32; ++kk)
+                mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+              // frees the stage and hands the accumulator over in both CTAs
+              mma_commit_pair_multicast(bar(L::EMPTY + s), 0x3);
+              mma_commit_pair_multicast(bar(L::T_FULL + b), 0x3);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BLOCK_K / 32; ++kk)
+                mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+              mma_commit(bar(L::EMPTY + s));
+              mma_commit(bar(L::T_FULL + b));
+            }
           }
           if (++s == STAGES) { s = 0; ph ^= 1; }
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
         }
       }
       // nothing issued may still run when the TMEM is freed
-      mma_commit(bar(L::MMA_DONE));
+      if constexpr (PAIR) mma_commit_pair_multicast(bar(L::MMA_DONE), 0x1);
+      else mma_commit(bar(L::MMA_DONE));
       drain_wait(bar(L::MMA_DONE), 0, p);
     }
     __syncwarp();
@@ -390,7 +432,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
     float acc[HALF];
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
-      const Tile T = decode_tile<BN, MODE>(t, p, num_m_blocks, prefix, mcnt);
+      const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
       // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
       if (!T.skip) {
@@ -437,7 +479,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(bar(L::T_EMPTY + b));
+            // pair form: the accumulator is released on the leader's barrier
+            if (PAIR && !leader) mbar_arrive_remote_relaxed(bar(L::T_EMPTY + b), 0);
+            else mbar_arrive(bar(L::T_EMPTY + b));
             mbar_arrive(bar(L::SA_EMPTY + j));
           }
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
@@ -482,7 +526,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         if (MODE != kMasked || T.rows == BLOCK_M) {
           // the store clips at the tensor's bounds (M rows, N columns)
-          if (pt == 0 && !*abort_flag) {
+          if (pt == 0 && !*abort_flag && T.rows > 0) {
             for (int cc = 0; cc < BN / 32; ++cc)
               if (T.n0 + cc * 32 < p.N)
                 tma_store_3d(&tmD, out_s + cc * (BLOCK_M * 64), T.n0 + cc * 32, T.m0, T.z);
@@ -590,11 +634,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, L::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    else tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
   // no CTA leaves while a peer may still copy into it; every exchanged byte
   // has been consumed by now, so the rendezvous needs no memory ordering
-  if (SPLIT) cluster_sync_relaxed();
+  if (SPLIT || PAIR) cluster_sync_relaxed();
 }
 
 }  // namespace dgk

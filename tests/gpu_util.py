@@ -88,18 +88,22 @@ def run_masked(p, expected_m=None, fill=W.BF16_SENTINEL, masked_m=None):
 
 
 class forced_config:
-    """Context manager: force (block_n, split_k) for the launches inside.  A
-    configuration the library has no kernel for (for example a K split with
-    256-wide tiles and more than 64 rows) skips the test."""
+    """Context manager: force (block_n, split_k[, pair]) for the launches
+    inside (pair: -1 heuristic, 0 off, 1 on).  A configuration the library has
+    no kernel for (for example a K split with 256-wide tiles and more than 64
+    rows) skips the test."""
 
-    def __init__(self, block_n, split_k):
+    def __init__(self, block_n, split_k, pair=-1):
         self.cfg = (block_n, split_k)
+        self.pair = pair
 
     def __enter__(self):
         dg.debug_force_config(*self.cfg)
+        dg.debug_force_pair(self.pair)
 
     def __exit__(self, exc_type, exc, tb):
         dg.debug_force_config(0, 0)
-        if exc_type is dg.DGError and exc.status == 2 and self.cfg != (0, 0):
+        dg.debug_force_pair(-1)
+        if exc_type is dg.DGError and exc.status == 2 and (self.cfg != (0, 0) or self.pair >= 0):
             import pytest
             pytest.skip(f"no kernel for forced config {self.cfg}")

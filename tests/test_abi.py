@@ -131,7 +131,10 @@ def test_plan_config_heuristic(L):
     # prefill: enough tiles -> no split, wide tiles
     cfg = dg.plan_config(0, 4096, 7168, 7168, 1, 152)
     assert cfg["split_k"] == 1 and cfg["grid"] <= 152
-    assert cfg["num_tiles"] == 32 * ((7168 + cfg["block_n"] - 1) // cfg["block_n"])
+    assert cfg["num_tiles"] == (4096 // cfg["block_m"]) * ((7168 + cfg["block_n"] - 1) // cfg["block_n"])
+    assert cfg["block_m"] == (256 if cfg["pair"] else 128)
+    # the pair form is for M > 128 only (unless forced)
+    assert dg.plan_config(0, 128, 7168, 7168, 1, 152)["pair"] == 0
     for kind, m, g in ((1, 32768, 4), (2, 256, 8)):
         cfg = dg.plan_config(kind, m, 4096, 7168, g, 152)
         assert cfg["split_k"] == 1 and cfg["smem_bytes"] <= 232448
@@ -141,6 +144,11 @@ def test_plan_config_heuristic(L):
 
 def test_force_config_hook(L):
     try:
+        dg.debug_force_pair(1)
+        assert dg.plan_config(0, 4096, 4096, 1024, 1, 152)["pair"] == 1
+        dg.debug_force_pair(0)
+        assert dg.plan_config(0, 4096, 4096, 1024, 1, 152)["pair"] == 0
+        dg.debug_force_pair(-1)
         dg.debug_force_config(256, 0)
         assert dg.plan_config(0, 4096, 4096, 1024, 1, 152)["block_n"] == 256
         dg.debug_force_config(128, 4)
@@ -150,3 +158,4 @@ def test_force_config_hook(L):
             dg.debug_force_config(128, 9)
     finally:
         dg.debug_force_config(0, 0)
+        dg.debug_force_pair(-1)

@@ -143,3 +143,35 @@ def test_masked_small(cfg):
         v = int(mm[g])
         assert np.all(got[g, v:] == W.BF16_SENTINEL), f"group {g}: rows past masked_m written"
         U.assert_close(got[g, :v], want[g, :v], f"masked group {g}")
+
+
+PAIR_SHAPES = [
+    (64, 256, 512),       # the second CTA of the pair has no rows
+    (1, 16, 128),
+    (200, 400, 384),      # ragged M and N
+    (333, 2112, 256),     # 2112: last B scale block is 64 rows
+    (512, 528, 1024),
+    (2048, 4096, 256),    # 8 x 16 = 128 pair tiles: more than the resident pairs
+]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_dense_pair(shape):
+    """The CTA-pair form (cta_group::2 MMA over a 2-CTA cluster, 256-row tiles)."""
+    M, N, K = shape
+    p = W.dense_problem(M, N, K, seed=M * 3 + N * 5 + K)
+    with U.forced_config(256, 1, pair=1):
+        got = U.run_dense(p)
+    U.assert_close(got, dense_ref(p), f"dense pair {shape}")
+
+
+def test_dense_pair_off_matches():
+    """Pair form forced off on a shape the heuristic gives to the pair form."""
+    p = W.dense_problem(640, 768, 512, seed=77)
+    with U.forced_config(0, 0, pair=0):
+        a = U.run_dense(p)
+    with U.forced_config(0, 0, pair=1):
+        b = U.run_dense(p)
+    want = dense_ref(p)
+    U.assert_close(a, want, "pair off")
+    U.assert_close(b, want, "pair on")
