@@ -230,8 +230,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const bool leader = crank == 0;                // pair form: the CTA that issues the MMAs
   const int cluster_id = blockIdx.x / CL;
   const int num_clusters = gridDim.x / CL;
-  const int kbeg = static_cast<int>(static_cast<long long>(crank) * p.kb / S);
-  const int kend = static_cast<int>(static_cast<long long>(crank + 1) * p.kb / S);
+  // this CTA's K groups: a slice of them in the split form, all of them otherwise
+  // (the pair form's cluster rank names a half of the tile, not of K)
+  const uint32_t krank = SPLIT ? crank : 0;
+  const int kbeg = static_cast<int>(static_cast<long long>(krank) * p.kb / S);
+  const int kend = static_cast<int>(static_cast<long long>(krank + 1) * p.kb / S);
   const int kcnt = kend - kbeg;
 
   // ------------------------------------------------------------- set-up --
@@ -333,12 +336,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if constexpr (PAIR) {
               // both CTAs' loads complete on the leader's FULL barrier, which
               // expects the bytes of both
+              // (destinations as cluster addresses of this CTA's own shared memory)
               const uint32_t full = map_cluster(bar(L::FULL + s), 0);
               if (leader) mbar_arrive_expect_tx(bar(L::FULL + s), 2 * (L::A_BYTES + L::B_BYTES));
-              tma_load_3d_pair(sbase + L::A_OFF + s * L::A_BYTES, &tmA, full, g * BLOCK_K, T.m0,
-                               T.z);
-              tma_load_3d_pair(sbase + L::B_OFF + s * L::B_BYTES, &tmB, full, g * BLOCK_K,
-                               T.n0 + static_cast<int>(crank) * (BN / 2), T.e);
+              tma_load_3d_pair(map_cluster(sbase + L::A_OFF + s * L::A_BYTES, crank), &tmA, full,
+                               g * BLOCK_K, T.m0, T.z);
+              tma_load_3d_pair(map_cluster(sbase + L::B_OFF + s * L::B_BYTES, crank), &tmB, full,
+                               g * BLOCK_K, T.n0 + static_cast<int>(crank) * (BN / 2), T.e);
             } else {
               mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + L::B_BYTES);
               tma_load_3d(sbase + L::A_OFF + s * L::A_BYTES, &tmA, bar(L::FULL + s), g * BLOCK_K,
