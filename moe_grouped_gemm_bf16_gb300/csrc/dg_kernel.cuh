@@ -254,7 +254,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     mbar_init(bar(L::RED_FULL), 1);
     mbar_init(bar(L::READY), S);
-    mbar_init(bar(L::MMA_DONE), 1);
+    mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
     misc[1] = 0;
     fence_mbarrier_init();
   }
@@ -279,7 +279,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // start their own prologue from here on.
   grid_dep_wait();
   grid_dep_launch_dependents();
-  if (MODE == kMasked && warp == 2) {  // (warp 2 is otherwise idle)
+  if (MODE == kMasked && warp == 2) {  // (warp 2 has no other set-up work)
     // valid rows per group (clamped to [0, max_m]) and the prefix sum of M blocks
     int carry = 0;
     for (int base = 0; base < p.num_groups; base += 32) {
@@ -376,17 +376,40 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if ((sa_issued_mask >> q) & 1u) drain_wait(bar(L::SA_FULL + q), (sa_issued_par >> q) & 1u, p);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer ---
+  } else if (warp <= NUM_ISSUERS) {
+    // ------------------------------------------------------ MMA issuers ---
+    // A thread that issues tcgen05.mma stalls until the tensor pipe takes the
+    // instruction, so the barrier waits between one K group's MMAs and the
+    // next would leave the pipe idle.  Warps 1..NUM_ISSUERS take the K groups
+    // in turn: while one waits for its stage and accumulator, another's MMAs
+    // run.  Group g goes to issuer g mod NUM_ISSUERS.
+    // The parity waits stay exact: (1) NUM_ISSUERS divides NBUF, so the issuer
+    // of group g also issued group g - NBUF on the same accumulator buffer and
+    // saw its release phase before, which rules out a barrier two phases behind;
+    // (2) STAGES >= NBUF, so once the accumulator of g - NBUF is released (the
+    // promotion runs in group order) the MMAs of every group up to g - NBUF,
+    // g - STAGES among them, have completed, and the stage's previous fill
+    // phase is over.  With an issuer count that does not divide NBUF a wait can
+    // pass a phase early and the barrier accounting breaks down.
     // (pair form: the leader issues for both CTAs; the other CTA's warp 1 only
     // takes part in the collective TMEM allocation)
+    static_assert(L::NBUF % NUM_ISSUERS == 0 && STAGES >= L::NBUF,
+                  "issuer turns must keep every barrier within one phase");
     if (lane == 0 && (!PAIR || leader)) {
-      int s = 0, b = 0;
+      const int me = warp - 1;
+      int s = 0, b = 0, turn = 0;
       uint32_t ph = 0, bph = 0;
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
         const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
         if (T.skip) continue;
         for (int g = kbeg; g < kend; ++g) {
+          const bool mine = (turn == me);
+          if (++turn == NUM_ISSUERS) turn = 0;
+          if (!mine) {
+            if (++s == STAGES) { s = 0; ph ^= 1; }
+            if (++b == L::NBUF) { b = 0; bph ^= 1; }
+            continue;
+          }
           const bool ok_t = wait_bar(bar(L::T_EMPTY + b), bph ^ 1, abort_flag, p);
           tc_fence_after();
           const bool ok_f = wait_bar(bar(L::FULL + s), ph, abort_flag, p);
@@ -453,6 +476,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!T.skip) {
         const int nmod = T.n0 & 127;
         for (int g = kbeg; g < kend; ++g) {
+          // hand the TMEM accumulator back to the MMA issuer (pair form: on the
+          // leader's barrier); every tcgen05.ld of this warp has completed
+          auto release_tmem = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (PAIR && !leader) mbar_arrive_remote_relaxed(bar(L::T_EMPTY + b), 0);
+              else mbar_arrive(bar(L::T_EMPTY + b));
+            }
+          };
           wait_bar(bar(L::T_FULL + b), bph, abort_flag, p);
           wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
           __syncwarp();
@@ -462,32 +495,38 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const float a_s = sa_ring[j * BLOCK_M + row];
           const float* sbg = sb_s + (g - kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
-          // 32-column chunks, software-pipelined: the load of chunk c+1 is in
-          // flight while chunk c is scaled and accumulated
-          uint32_t v[2][32];
-          tmem_ld_32x32b_x32(tcol, v[0]);
-          tmem_wait_ld(v[0]);
+          // Two 32-column chunks per load batch: tcgen05.wait::ld waits for every
+          // outstanding load, so fewer, larger batches expose its latency fewer
+          // times.  The accumulator is released as soon as the last batch is in
+          // registers, before that batch is scaled and added.
+          constexpr int LB = 2;
+          constexpr int NB = NCH / LB;
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            if (c + 1 < NCH) tmem_ld_32x32b_x32(tcol + (c + 1) * 32, v[(c + 1) & 1]);
-            const int col = h * HALF + c * 32;
-            // the 32 columns lie in one 128-column B scale block
-            const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
+          for (int bt = 0; bt < NB; ++bt) {
+            uint32_t v[LB][32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], __uint_as_float(v[c & 1][i]),
-                    __uint_as_float(v[c & 1][i + 1]), sc);
-            if (c + 1 < NCH) tmem_wait_ld(v[(c + 1) & 1]);
+            for (int u = 0; u < LB; ++u)
+              tmem_ld_32x32b_x32(tcol + (bt * LB + u) * 32, v[u]);
+#pragma unroll
+            for (int u = 0; u < LB; ++u) tmem_wait_ld(v[u]);
+            if (bt == NB - 1) release_tmem();
+#pragma unroll
+            for (int u = 0; u < LB; ++u) {
+              const int c = bt * LB + u;
+              const int col = h * HALF + c * 32;
+              // the 32 columns lie in one 128-column B scale block
+              const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2)
+                ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], __uint_as_float(v[u][i]),
+                      __uint_as_float(v[u][i + 1]), sc);
+            }
           }
+          } else {
+            release_tmem();
           }
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            // pair form: the accumulator is released on the leader's barrier
-            if (PAIR && !leader) mbar_arrive_remote_relaxed(bar(L::T_EMPTY + b), 0);
-            else mbar_arrive(bar(L::T_EMPTY + b));
-            mbar_arrive(bar(L::SA_EMPTY + j));
-          }
+          if (lane == 0) mbar_arrive(bar(L::SA_EMPTY + j));
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
           if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
         }

@@ -10,8 +10,14 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
 
 constexpr int BLOCK_M = 128;  // rows of A per tile (one tcgen05 M=128 MMA)
 constexpr int BLOCK_K = 128;  // one K group: the granularity of both scale factors
-constexpr int NUM_THREADS = 384;  // warpgroup 0: warp 0 TMA, warp 1 MMA; warpgroups 1-2: promotion
+constexpr int NUM_THREADS = 384;  // warpgroup 0: warp 0 TMA, warps 1.. MMA; warpgroups 1-2: promotion
 constexpr int NUM_PROMO_WARPS = 8;
+// MMA issuer warps (warps 1..NUM_ISSUERS of warpgroup 0), taking K groups in turn
+#ifndef DG_NUM_ISSUERS
+#define DG_NUM_ISSUERS 2
+#endif
+constexpr int NUM_ISSUERS = DG_NUM_ISSUERS;
+static_assert(NUM_ISSUERS == 1 || NUM_ISSUERS == 2, "the issuer count must divide every NBUF");
 constexpr int SA_SLOTS = 8;   // depth of the activation-scale ring
 constexpr int MAX_GROUPS_MASKED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
