@@ -106,48 +106,51 @@ struct Plan {
   int smem = 0;
 };
 
-// Estimated kernel time (us) of one configuration, from measured GB300
-// figures: a 128-deep K group of tcgen05.mma (M=128) takes ~454 cycles for
-// N <= 128 and ~643 cycles for N = 256 (dependent-accumulate floor and tensor
-// throughput); a TMA load round trip under load is ~1.6 us; HBM ~6.5 TB/s.
+// Estimated kernel time (us) of one configuration.  The constants are fitted
+// to timings of every configuration of the dense decode and prefill sweeps on
+// GB300 (median error ~8%):
+//  * a CTA's K group costs the slowest of: the MMA/promotion cadence (0.22 us
+//    for 128-wide tiles, 0.50 us for 256-wide, 0.39 us for a CTA pair's
+//    256 x 256 tile), its share of HBM bandwidth for the B tile (~9 TB/s
+//    aggregate, L2 hits included), and the SM's TMA ingest for A and B
+//    (~100 GB/s per SM);
+//  * each wave of CTAs pays ~3 us before its first operands land and a tail
+//    (~4.9 us for the K split's cluster reduction, ~1.6 us otherwise);
+//  * a persistent CTA pays ~0.9 us per extra tile (epilogue), plus ~1.9 us per
+//    launch.
+// A split whose clusters do not all fit at once runs in several waves, each
+// paying its own head and tail: this is what the model must steer away from.
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
-  const double ghz = 2.0;
-  double t_mma = (in.block_n <= 128 ? 454.0 : 643.0 * in.block_n / 256.0) / (ghz * 1e3);
-  // operand delivery: each K group brings (A rows + B rows this CTA loads) x 128
-  // bytes at ~120 GB/s per SM, and shares shared-memory bandwidth with the MMA
-  const double b_rows = in.pair ? in.block_n / 2.0 : (double)in.block_n;
-  const double t_in = (in.a_rows + b_rows) * 128.0 / 120e3;
-  t_mma = std::max(t_mma, t_in);
+  (void)kind; (void)n; (void)num_groups;
+  const double t_cad = in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
+  const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
+  const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
+  const double head = 3.06, tail = S > 1 ? 4.9 : 1.6, per_tile = 0.92, fixed = 1.9;
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
-  long long ctas, rounds;
+  const double a_rows = (in.a_rows < 128 || m_rows <= 64) ? std::min<long long>(in.a_rows, 64) : 128.0;
+  const double b_rows = in.pair ? in.block_n / 2.0 : (double)in.block_n;
+  long long ctas, waves = 1, groups, ntile = 1;
   if (in.split) {
-    // one cluster per tile, as many waves as the resident clusters need
-    rounds = cdiv(tiles, clusters_resident);
-    ctas = std::min<long long>(tiles, clusters_resident) * S;
+    const long long cl = std::max<long long>(1, std::min(tiles, clusters_resident));
+    waves = cdiv(tiles, std::max<long long>(1, clusters_resident));
+    ctas = cl * S;
+    groups = kper;
   } else if (in.pair) {
-    // tiles are 256 rows, one per CTA pair
-    const long long pairs = std::max<long long>(1, std::min<long long>(tiles, clusters_resident));
+    const long long pairs = std::max<long long>(1, std::min(tiles, clusters_resident));
     ctas = 2 * pairs;
-    rounds = cdiv(tiles, pairs);
+    ntile = cdiv(tiles, pairs);
+    groups = ntile * kb;
   } else {
-    ctas = std::min<long long>(tiles, num_sms);
-    rounds = cdiv(tiles, ctas);  // tiles one persistent CTA computes in turn
+    ctas = std::max<long long>(1, std::min<long long>(tiles, num_sms));
+    ntile = cdiv(tiles, ctas);
+    groups = ntile * kb;
   }
-  const double t_comp = (double)rounds * kper * t_mma;
-  // unique HBM bytes: operands once, output once
-  const double groups = (kind == dgk::kDense) ? 1.0 : (double)num_groups;
-  const double m_all = (kind == dgk::kMasked) ? (double)num_groups * m_rows : (double)m_rows;
-  const double bytes = m_all * k + groups * (double)n * k + 2.0 * m_all * n;
-  // bytes in flight bound the bandwidth a wave can draw
-  const double stage_b = (double)in.block_n * 128.0;
-  const double bw = std::min(6.5e6, (double)ctas * in.stages * stage_b / 1.6);  // bytes/us
-  const double t_mem = bytes / bw;
-  const double fixed = 2.0 + (double)rounds * (S > 1 ? 1.5 : 0.6);
-  // the MMA issue and the loads overlap only in part (measured per-group
-  // cadence: MMA time plus a share of the load wait)
-  return std::max(t_comp, t_mem) + 0.5 * std::min(t_comp, t_mem) + fixed;
+  const double t_mem = b_rows * 128.0 / (bw_hbm / (double)ctas);
+  const double t_tma = (a_rows + b_rows) * 128.0 / bw_sm;
+  const double tg = std::max(t_cad, std::max(t_mem, t_tma));
+  return fixed + (double)waves * (head + (double)groups * tg + tail) + (double)(ntile - 1) * per_tile;
 }
 
 bool has_split64(const Table& tab) {
@@ -169,11 +172,12 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     if (force_bn > 0 && in.block_n != force_bn) continue;
     // 64-row A tiles serve M <= 64 only, and are the choice there
     if (in.a_rows < 128 && m_rows > in.a_rows) continue;
-    // 256-row pair tiles only pay off with more than one 128-row block
+    // The CTA-pair form measured slower than the 128-row form on every shape
+    // so far (its promotion, not the MMA, sets the pace): it runs only when
+    // forced.
     const int fp = g_force_pair.load();
-    if (fp == 0 && in.pair) continue;
+    if (fp <= 0 && in.pair) continue;
     if (fp == 1 && !in.pair) continue;
-    if (fp < 0 && in.pair && m_rows <= 128) continue;
     if (in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;

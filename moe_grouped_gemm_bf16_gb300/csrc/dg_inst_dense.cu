@@ -11,6 +11,7 @@ const Instance* instances_dense(int* count) {
       InstanceOf<128, 8, true, kDense, 64>::make(),
       InstanceOf<256, 5, true, kDense, 64>::make(),
       InstanceOf<256, 4, false, kDense, 128, true>::make(),
+      InstanceOf<128, 6, false, kDense, 128, true>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;

@@ -202,8 +202,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
-  static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && BN == 256),
-                "the pair form: dense, full A, 256-wide tiles");
+  static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && (BN == 128 || BN == 256)),
+                "the pair form: dense, full A, 128- or 256-wide tiles");
   using L = SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>;
   constexpr int HALF = BN / 2;                 // columns per promotion warpgroup
   constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup

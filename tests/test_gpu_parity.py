@@ -156,11 +156,12 @@ PAIR_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_dense_pair(shape):
+@pytest.mark.parametrize("bn", [256, 128], ids=lambda b: f"bn{b}")
+def test_dense_pair(shape, bn):
     """The CTA-pair form (cta_group::2 MMA over a 2-CTA cluster, 256-row tiles)."""
     M, N, K = shape
     p = W.dense_problem(M, N, K, seed=M * 3 + N * 5 + K)
-    with U.forced_config(256, 1, pair=1):
+    with U.forced_config(bn, 1, pair=1):
         got = U.run_dense(p)
     U.assert_close(got, dense_ref(p), f"dense pair {shape}")
 
