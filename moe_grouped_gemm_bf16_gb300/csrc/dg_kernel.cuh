@@ -306,7 +306,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (SPLIT || PAIR) cluster_sync();
+  // peers signal this CTA's barriers from here on: thread 0 made their
+  // initialisation visible to the cluster (fence.mbarrier_init), so a relaxed
+  // rendezvous suffices
+  if (SPLIT || PAIR) {
+    cluster_arrive_relaxed();
+    cluster_wait();
+  }
   const uint32_t tmem_base = misc[0];
   const int num_m_blocks = (MODE == kMasked) ? prefix[p.num_groups] : p.num_m_blocks;
   const int num_tiles = num_m_blocks * p.num_n_blocks;
@@ -444,6 +450,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     __syncwarp();
   }
+  // (K split: these warps touch no peer's memory; their part of the final
+  // cluster rendezvous is done)
+  if constexpr (SPLIT) cluster_arrive_relaxed();
   } else {
     if constexpr (REALLOC) regs_inc<232>();
     // -------------------------------------------------- promotion warps ---
@@ -457,6 +466,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int b = 0, j = 0;
     uint32_t bph = 0, jph = 0;
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
+    bool arrived = false;               // K split: arrived on the final cluster barrier
     float acc[HALF];
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
@@ -635,7 +645,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                  map_cluster(bar(L::RED_FULL), o));
           }
         }
-        wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
+        const bool red_ok = wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
+        // every byte sent to this CTA has landed, and the sum below reads only
+        // this CTA's memory: its part of the final cluster rendezvous is done.
+        // (The copies this CTA sent read its staging until their receivers'
+        // RED_FULL completes; the rendezvous before exit waits for all of them.)
+        if (red_ok && !arrived) {
+          cluster_arrive_relaxed();
+          arrived = true;
+        }
         __syncwarp();
         constexpr int UPR = BN / 4;  // 16-byte units per row
         for (int i = pt; i < own_rows * UPR; i += 32 * NUM_PROMO_WARPS) {
@@ -664,10 +682,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(T.m0 + grow) * p.N + n) = w;
           }
         }
-        // every byte sent to this CTA has landed before it may exit
-        if (pt == 0) drain_wait(bar(L::RED_FULL), 0, p);
+        // after an abort: every byte sent to this CTA lands before it may exit
+        if (!red_ok) drain_wait(bar(L::RED_FULL), 0, p);
       }
     }  // tile loop
+    if constexpr (SPLIT) {
+      if (!arrived) cluster_arrive_relaxed();
+    }
     if (pt == 0) bulk_wait_group0();
     __syncwarp();
   }
@@ -680,9 +701,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if constexpr (PAIR) tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
     else tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
-  // no CTA leaves while a peer may still copy into it; every exchanged byte
-  // has been consumed by now, so the rendezvous needs no memory ordering
-  if (SPLIT || PAIR) cluster_sync_relaxed();
+  // no CTA leaves while a peer may still copy into it or read from it; every
+  // exchanged byte has landed by now, so the rendezvous needs no memory
+  // ordering.  (K split: each thread arrived when its part was done.)
+  if constexpr (SPLIT) cluster_wait();
+  else if constexpr (PAIR) cluster_sync_relaxed();
 }
 
 }  // namespace dgk
