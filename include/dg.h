@@ -121,9 +121,13 @@ const char* dg_last_error_string(void);
  * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE). */
 dg_status dg_get_device_status(void* stream);
 
-/* Tile configuration the library would choose (heuristic, host only; no device
- * needed).  kind: 0 dense, 1 contiguous, 2 masked.  m is M (dense), M_total
- * (contiguous) or expected_m (masked).  num_sms is the SM count to plan for. */
+/* Tile configuration the library would choose (heuristic; no device needed).
+ * kind: 0 dense, 1 contiguous, 2 masked.  m is M (dense), M_total
+ * (contiguous) or expected_m (masked).  num_sms is the SM count to plan for.
+ * With a GB300 as the current device (and num_sms at most its SM count), the
+ * clusters that fit at once are the device's, so the result is the
+ * configuration a launch on num_sms SMs takes; without one, num_sms / S
+ * clusters of S CTAs are assumed to fit. */
 typedef struct dg_config {
   int block_m;      /* output tile height: 128, or 256 in the CTA-pair form */
   int block_n;      /* output tile width */

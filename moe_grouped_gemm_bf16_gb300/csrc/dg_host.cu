@@ -567,7 +567,24 @@ dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_
       k > 128 * dgk::MAX_KB || num_sms < 1 || (kind != dgk::kDense && num_groups < 1))
     return fail(DG_ERR_INVALID_ARG, "dg_plan_config: bad arguments");
   const int G = kind == dgk::kDense ? 1 : num_groups;
-  auto cap = [&](int, const Instance&, int S, int) { return S <= 1 ? num_sms : num_sms / S; };
+  // With a GB300 as the current device, clusters fit as the device reports
+  // (the configuration a launch takes); otherwise num_sms / S clusters of S.
+  DeviceState* st = nullptr;
+  {
+    int cnt = 0, dev = 0, major = 0, minor = 0;
+    if (cudaGetDeviceCount(&cnt) == cudaSuccess && cnt > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        major == 10 && minor == 3) {
+      int d = -1;
+      if (device_state(&st, &d) != DG_OK || num_sms > st->sms) st = nullptr;
+    }
+    cudaGetLastError();
+  }
+  auto cap = [&](int i, const Instance& in, int S, int smem) {
+    if (S <= 1) return num_sms;
+    return st ? clusters_resident(*st, kind, i, in, S, smem, num_sms) : num_sms / S;
+  };
   const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load());
   if (pl.inst < 0) return fail(DG_ERR_UNSUPPORTED_SHAPE, "no configuration");
   const Instance& in = table_for(kind).p[pl.inst];

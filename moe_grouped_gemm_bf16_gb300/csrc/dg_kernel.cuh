@@ -205,7 +205,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && (BN == 128 || BN == 256)),
                 "the pair form: dense, full A, 128- or 256-wide tiles");
   using L = SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>;
-  constexpr int HALF = BN / 2;                 // columns per promotion warpgroup
+  constexpr int HALF = BN / PROMO_WG;          // columns per promotion warpgroup
   constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup
   // the pair MMA spans both CTAs' 128 rows
   constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BLOCK_M : BLOCK_M, BN);
@@ -320,13 +320,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // cluster per tile); the operand ring is reused by its epilogue
   const int tile_stride = SPLIT ? num_tiles : num_clusters;
 
-  // A 256-column tile needs 128 accumulator registers per promotion thread:
-  // move registers from warpgroup 0 (TMA, MMA, two idle warps) to the two
-  // promotion warpgroups.  Per SM sub-partition: 40 + 2 * 232 = 3 * 168.
-  constexpr bool REALLOC = (HALF >= 128);
+  // Move registers from warpgroup 0 (TMA, MMA issue, an idle warp) to the
+  // promotion warpgroups when their accumulators need them.  The shares add up
+  // to what the launch holds: two promotion warpgroups (384 threads, 168 each):
+  // 40 + 2 * 232 = 3 * 168; four (640 threads, 96 each): 32 + 4 * 112 = 5 * 96.
+  constexpr bool REALLOC = PROMO_WG == 4 || HALF >= 128;
+  constexpr uint32_t REGS_CTRL = PROMO_WG == 4 ? 32 : 40;
+  constexpr uint32_t REGS_PROMO = PROMO_WG == 4 ? 112 : 232;
+  static_assert(REGS_CTRL + PROMO_WG * REGS_PROMO <= (1 + PROMO_WG) * (PROMO_WG == 4 ? 96 : 168),
+                "register shares exceed the launch's registers");
 
   if (warp < 4) {
-  if constexpr (REALLOC) regs_dec<40>();
+  if constexpr (REALLOC) regs_dec<REGS_CTRL>();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && !(p.debug_flags & DBG_SKIP_PRODUCER)) {
@@ -450,23 +455,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     __syncwarp();
   }
-  // (K split: these warps touch no peer's memory; their part of the final
-  // cluster rendezvous is done)
-  if constexpr (SPLIT) cluster_arrive_relaxed();
   } else {
-    if constexpr (REALLOC) regs_inc<232>();
+    if constexpr (REALLOC) regs_inc<REGS_PROMO>();
     // -------------------------------------------------- promotion warps ---
-    const int pw = warp - 4;            // 0..7
+    const int pw = warp - 4;            // 0 .. NUM_PROMO_WARPS-1
     const int q = warp & 3;             // TMEM lane quadrant this warp may access
-    const int h = pw >> 2;              // which half of the tile's columns
+    const int h = pw >> 2;              // which column share of the tile
     const int row = q * 32 + lane;      // the tile row this thread owns
-    const int pt = threadIdx.x - 128;   // 0..255 among the promotion threads
+    const int pt = threadIdx.x - 128;   // index among the promotion threads
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t out_s = sbase + L::OUT_OFF;
     int b = 0, j = 0;
     uint32_t bph = 0, jph = 0;
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
-    bool arrived = false;               // K split: arrived on the final cluster barrier
     float acc[HALF];
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
@@ -505,12 +506,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const float a_s = sa_ring[j * BLOCK_M + row];
           const float* sbg = sb_s + (g - kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
-          // Two 32-column chunks per load batch: tcgen05.wait::ld waits for every
-          // outstanding load, so fewer, larger batches expose its latency fewer
-          // times.  The accumulator is released as soon as the last batch is in
-          // registers, before that batch is scaled and added.
-          constexpr int LB = 2;
+          // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
+          // every outstanding load, so fewer, larger batches expose its latency
+          // fewer times.  The accumulator is released as soon as the last batch
+          // is in registers, before that batch is scaled and added.
+          constexpr int LB = NCH < PROMO_LB ? NCH : PROMO_LB;
           constexpr int NB = NCH / LB;
+          static_assert(NCH % LB == 0, "whole load batches");
 #pragma unroll
           for (int bt = 0; bt < NB; ++bt) {
             uint32_t v[LB][32];
@@ -646,14 +648,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
         }
         const bool red_ok = wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
-        // every byte sent to this CTA has landed, and the sum below reads only
-        // this CTA's memory: its part of the final cluster rendezvous is done.
-        // (The copies this CTA sent read its staging until their receivers'
-        // RED_FULL completes; the rendezvous before exit waits for all of them.)
-        if (red_ok && !arrived) {
-          cluster_arrive_relaxed();
-          arrived = true;
-        }
         __syncwarp();
         constexpr int UPR = BN / 4;  // 16-byte units per row
         for (int i = pt; i < own_rows * UPR; i += 32 * NUM_PROMO_WARPS) {
@@ -686,9 +680,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (!red_ok) drain_wait(bar(L::RED_FULL), 0, p);
       }
     }  // tile loop
-    if constexpr (SPLIT) {
-      if (!arrived) cluster_arrive_relaxed();
-    }
     if (pt == 0) bulk_wait_group0();
     __syncwarp();
   }
@@ -701,11 +692,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if constexpr (PAIR) tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
     else tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
-  // no CTA leaves while a peer may still copy into it or read from it; every
+  // No CTA leaves while a peer may still copy into it or read from it; every
   // exchanged byte has landed by now, so the rendezvous needs no memory
-  // ordering.  (K split: each thread arrived when its part was done.)
-  if constexpr (SPLIT) cluster_wait();
-  else if constexpr (PAIR) cluster_sync_relaxed();
+  // ordering.  All of a cluster's CTAs leave together: letting each thread
+  // arrive as soon as its own part was done (and the sum overlap the peers'
+  // skew) made back-to-back launches of 5-CTA clusters take a second wave
+  // (decode 64x7168x16384, split 5: 29.5 -> 43 us).
+  if (SPLIT || PAIR) cluster_sync_relaxed();
 }
 
 }  // namespace dgk

@@ -10,8 +10,20 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
 
 constexpr int BLOCK_M = 128;  // rows of A per tile (one tcgen05 M=128 MMA)
 constexpr int BLOCK_K = 128;  // one K group: the granularity of both scale factors
-constexpr int NUM_THREADS = 384;  // warpgroup 0: warp 0 TMA, warps 1.. MMA; warpgroups 1-2: promotion
-constexpr int NUM_PROMO_WARPS = 8;
+// Promotion warpgroups (each covers all 128 tile rows and 1/PROMO_WG of the
+// columns).  Warpgroup 0: warp 0 TMA, warps 1.. MMA issue.
+#ifndef DG_PROMO_WG
+#define DG_PROMO_WG 2
+#endif
+constexpr int PROMO_WG = DG_PROMO_WG;
+static_assert(PROMO_WG == 2 || PROMO_WG == 4, "two or four promotion warpgroups");
+constexpr int NUM_THREADS = 128 * (1 + PROMO_WG);
+constexpr int NUM_PROMO_WARPS = 4 * PROMO_WG;
+// 32-column TMEM chunks a promotion warp loads per tcgen05.wait::ld
+#ifndef DG_PROMO_LB
+#define DG_PROMO_LB 2
+#endif
+constexpr int PROMO_LB = DG_PROMO_LB;
 // MMA issuer warps (warps 1..NUM_ISSUERS of warpgroup 0), taking K groups in turn
 #ifndef DG_NUM_ISSUERS
 #define DG_NUM_ISSUERS 2
