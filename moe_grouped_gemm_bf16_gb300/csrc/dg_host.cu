@@ -129,7 +129,8 @@ double est_time_us(const Instance& in, int S, long long tiles, long long cluster
   const double head = 3.06, tail = S > 1 ? 4.9 : 1.6, per_tile = 0.92, fixed = 1.9;
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
-  const double a_rows = (in.a_rows < 128 || m_rows <= 64) ? std::min<long long>(in.a_rows, 64) : 128.0;
+  // the A box the TMA fills per K group (rows past M are zero-filled, not free)
+  const double a_rows = in.a_rows;
   const double b_rows = in.pair ? in.block_n / 2.0 : (double)in.block_n;
   long long ctas, waves = 1, groups, ntile = 1;
   if (in.split) {
@@ -351,7 +352,7 @@ dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, co
   {
     const uint64_t dims[3] = {(uint64_t)ld_sa, (uint64_t)kb, (uint64_t)zA};
     const uint64_t str[2] = {(uint64_t)ld_sa * 4, (uint64_t)kb * ld_sa * 4};
-    const uint32_t box[3] = {128, 1, 1};
+    const uint32_t box[3] = {128, (uint32_t)dgk::SA_GROUPS, 1};
     dg_status s = encode(&mp->sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(sa), dims,
                          str, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                          "sa");

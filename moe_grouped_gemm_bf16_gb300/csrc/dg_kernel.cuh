@@ -46,7 +46,7 @@ template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false
 struct SmemLayout {
   static constexpr int A_BYTES = AROWS * BLOCK_K;    // e4m3 A slot (16 KB or 8 KB)
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BLOCK_K;
-  static constexpr int SA_BYTES = BLOCK_M * 4;       // 512 B fp32
+  static constexpr int SA_BYTES = SA_GROUPS * BLOCK_M * 4;  // [SA_GROUPS][128] fp32
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
   static constexpr int SA_OFF = B_OFF + STAGES * B_BYTES;
@@ -364,15 +364,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             issued_mask |= 1u << s;
             issued_par = (issued_par & ~(1u << s)) | (ph << s);
           }
-          if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
-            mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
-            tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0, g,
-                        T.z);
-            sa_issued_mask |= 1u << j;
-            sa_issued_par = (sa_issued_par & ~(1u << j)) | (jph << j);
+          // the scales of this and the next SA_GROUPS-1 K groups (groups past
+          // the tensor's end read as zero and are not used)
+          if ((g - kbeg) % SA_GROUPS == 0) {
+            if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
+              mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
+              tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
+                          g, T.z);
+              sa_issued_mask |= 1u << j;
+              sa_issued_par = (sa_issued_par & ~(1u << j)) | (jph << j);
+            }
+            if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
           }
           if (++s == STAGES) { s = 0; ph ^= 1; }
-          if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
         }
       }
       // Drain: after an abort the latest load into a slot may still be in
@@ -497,13 +501,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               else mbar_arrive(bar(L::T_EMPTY + b));
             }
           };
+          const int r = (g - kbeg) % SA_GROUPS;   // place in the scale slot
           wait_bar(bar(L::T_FULL + b), bph, abort_flag, p);
-          wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
+          if (r == 0) wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
           __syncwarp();
           tc_fence_after();
           // warps whose TMEM lanes hold no loaded row of A have nothing to add
           if (q * 32 < AROWS) {
-          const float a_s = sa_ring[j * BLOCK_M + row];
+          const float a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
           const float* sbg = sb_s + (g - kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
@@ -537,10 +542,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           } else {
             release_tmem();
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::SA_EMPTY + j));
+          if (r == SA_GROUPS - 1 || g == kend - 1) {
+            // the slot's last K group of this tile: hand the slot back
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::SA_EMPTY + j));
+            if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+          }
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
-          if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
         }
       }
       if constexpr (!SPLIT) {

@@ -30,7 +30,10 @@ constexpr int PROMO_LB = DG_PROMO_LB;
 #endif
 constexpr int NUM_ISSUERS = DG_NUM_ISSUERS;
 static_assert(NUM_ISSUERS == 1 || NUM_ISSUERS == 2, "the issuer count must divide every NBUF");
-constexpr int SA_SLOTS = 8;   // depth of the activation-scale ring
+// Activation-scale ring: each slot holds the scales of SA_GROUPS consecutive K
+// groups (one TMA load, one full/empty barrier round trip per slot)
+constexpr int SA_GROUPS = 4;
+constexpr int SA_SLOTS = 4;
 constexpr int MAX_GROUPS_MASKED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
 constexpr int MAX_SPLIT = 8;  // CTAs per cluster in the K-split form
