@@ -25,6 +25,12 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
                    identity, linearity/transpose, float64 library closed form
   grouped_*        pinned: equal to per-expert / per-group dense runs,
                    padding rows +0 and masked rows untouched (bit-exact)
+  e4m3_from_float  pinned: torch's float32 -> float8_e4m3fn cast (after
+                   clamping to +-448) on every code value, every midpoint
+                   between neighbours (ties), saturation and random values
+  quantize_1x128   pinned: the group maximum maps to code magnitude 448, the
+                   scale times 448 recovers the maximum, every code decodes
+                   to x / scale within half an e4m3 step, zero groups, layout
 """
 import ctypes
 import os
@@ -60,8 +66,12 @@ def _load(path):
                                                    _u16p, _int, _int, _int, _i64p, _int, _int]
     lib.dg_ref_grouped_masked.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _i32p, _u16p,
                                           _int, _int, _int, _int, _int]
+    lib.dg_ref_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.dg_ref_e4m3_from_float.restype = ctypes.c_uint8
+    lib.dg_ref_quantize_1x128.argtypes = [_u16p, _u8p, _f32p, _int, _int, _int, _int, _int]
     for f in ("dg_ref_gemm_nt_f64", "dg_ref_gemm_nt", "dg_ref_gemm_nt_rows",
-              "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked"):
+              "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked",
+              "dg_ref_quantize_1x128"):
         getattr(lib, f).restype = None
     return lib
 
@@ -97,6 +107,9 @@ class Oracle:
 
     def bf16_rne(self, x):
         return int(self.lib.dg_ref_bf16_rne(float(x)))
+
+    def e4m3_from_float(self, v):
+        return int(self.lib.dg_ref_e4m3_from_float(float(np.float32(v))))
 
     def max_threads(self):
         return int(self.lib.dg_ref_max_threads())
@@ -176,6 +189,26 @@ class Oracle:
                                        _p(sb, _f32p), _p(masked_m, _i32p), _p(D, _u16p),
                                        G, max_m, N, K, nthreads)
         return D
+
+
+    # -- activation quantiser (the step that produces A and sa) -------------
+    def quantize_1x128(self, X, ld_sa=None, sa_fill=np.nan, nthreads=0):
+        """X: bf16 bit patterns [M,K] or [G,M,K] (uint16).  Returns (Q, sa):
+        e4m3 codes of X's shape, and fp32 scales [kb, ld_sa] ([G, kb, ld_sa]);
+        scale columns m >= M keep `sa_fill`."""
+        X = _c(X, np.uint16)
+        squeeze = X.ndim == 2
+        if squeeze:
+            X = X[None]
+        G, M, K = X.shape
+        assert K % 128 == 0
+        ld_sa = M if ld_sa is None else int(ld_sa)
+        assert ld_sa >= M
+        Q = np.zeros((G, M, K), np.uint8)
+        sa = np.full((G, K // 128, ld_sa), sa_fill, np.float32)
+        self.lib.dg_ref_quantize_1x128(_p(X, _u16p), _p(Q, _u8p), _p(sa, _f32p), G, M, K, ld_sa,
+                                       nthreads)
+        return (Q[0], sa[0]) if squeeze else (Q, sa)
 
 
 def _check_dense(A, sa, B, sb):

@@ -15,7 +15,8 @@ LIB = os.path.join(HERE, "libdgref.so")
 
 
 def _compile(out, defines=()):
-    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", SRC, "-o", out, "-lm"]
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-std=c11", SRC,
+           "-o", out, "-lm"]
     cmd[1:1] = [f"-D{d}" for d in defines]
     subprocess.run(cmd, check=True)
     return out

@@ -28,6 +28,9 @@
  * round in double (relative error ~1e-16).  The result is rounded once, from
  * double straight to bf16, round-to-nearest-even.
  *
+ * The file also holds the activation quantiser that produces A and sa
+ * (dg_ref_quantize_1x128, at the end, with its own reading).
+ *
  * The M-grouped forms (same pages, section "Dense y Grouped GEMM"):
  *  - contiguous: rows of all experts are concatenated along M; m_indices[m]
  *    names the expert of row m, and -1 marks a padding row, whose output is
@@ -308,6 +311,106 @@ void dg_ref_grouped_masked(const uint8_t *A, const float *sa, int ld_sa,
             for (int n = 0; n < N; ++n)
                 drow[n] = dg_ref_bf16_rne(acc[n]);
             free(acc);
+        }
+    }
+}
+
+/* ------------------------------------------------ activation quantiser -- */
+/* The step that produces the GEMM's left operand: each row of a bf16
+ * activation matrix is cut into 128-wide K groups, and each (row, group) gets
+ * one fp32 scale and 128 e4m3 codes.  The pages state the layout of the
+ * result (the LHS scales fp32 and K-group-major, "transposed", TMA-aligned:
+ * es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de layout")
+ * and, in the same section, leave the FP8 conversion to the caller, without
+ * fixing its arithmetic.  The reading taken here, all in fp32:
+ *
+ *   amax     = max |x[m,k]| over the group              (exact)
+ *   a        = max(amax, 1e-4)
+ *   sa[g][m] = a / 448                                   (fp32 division)
+ *   q[m,k]   = e4m3_rne_satfinite( x[m,k] * (448 / a) )   (fp32 division once,
+ *                                                          fp32 multiply each)
+ *
+ * 448 is the largest finite e4m3 value, so the largest |x| of a group maps to
+ * code magnitude 448.  Inputs are finite. */
+
+/* fp32 -> e4m3 ("fn"): round to nearest, ties to even, saturating to +-448
+ * (the format has no infinity); NaN gives 0x7F.  Written from the format
+ * definition: normal values (1 + f/8) * 2^(e-7) have spacing 2^(E-3) in
+ * [2^E, 2^(E+1)); below 2^-6 the spacing stays 2^-9 (subnormals). */
+uint8_t dg_ref_e4m3_from_float(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs((double)v);          /* exact */
+    uint8_t code;
+    if (a >= 448.0) {
+        code = 0x7E;                     /* saturate: S.1111.110 = 448 */
+    } else if (a < ldexp(1.0, -6)) {
+        /* subnormal range; n = 8 is the smallest normal value, code 0x08 */
+#if DG_REF_MUTANT == 12
+        double n = floor(a / ldexp(1.0, -9));    /* mutant: truncation */
+#else
+        double n = nearbyint(a / ldexp(1.0, -9));
+#endif
+        code = (uint8_t)n;
+    } else {
+        int ex;
+        frexp(a, &ex);                   /* a in [2^(ex-1), 2^ex) */
+        int E = ex - 1;
+#if DG_REF_MUTANT == 12
+        double n = floor(a / ldexp(1.0, E - 3)); /* mutant: truncation */
+#else
+        double n = nearbyint(a / ldexp(1.0, E - 3));   /* 8..16, exact division */
+#endif
+        if (n >= 16.0) {                 /* rounded up into the next binade */
+            E += 1;
+            n = 8.0;
+        }
+        code = (uint8_t)(((E + 7) << 3) | ((int)n - 8));   /* a < 448: E <= 8 */
+    }
+    return neg ? (uint8_t)(code | 0x80) : code;
+}
+
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* X: bf16 bit patterns [G][M][K]; Q: e4m3 codes [G][M][K];
+ * sa: [G][K/128][ld_sa], columns m < M written. */
+void dg_ref_quantize_1x128(const uint16_t *X, uint8_t *Q, float *sa, int num_groups, int M,
+                           int K, int ld_sa, int nthreads)
+{
+    int kb = K / 128;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int z = 0; z < num_groups; ++z) {
+        for (int m = 0; m < M; ++m) {
+            for (int g = 0; g < kb; ++g) {
+                const uint16_t *x = X + ((size_t)z * M + m) * K + (size_t)g * 128;
+                uint8_t *q = Q + ((size_t)z * M + m) * K + (size_t)g * 128;
+                float amax = 0.0f;
+                for (int k = 0; k < 128; ++k) {
+                    float v = fabsf(bf16_bits_to_float(x[k]));
+                    if (v > amax)
+                        amax = v;
+                }
+                float a = amax > 1e-4f ? amax : 1e-4f;
+#if DG_REF_MUTANT == 11
+                float scale = a;                  /* mutant: 448 left out */
+                float factor = 1.0f / a;
+#else
+                float scale = a / 448.0f;
+                float factor = 448.0f / a;
+#endif
+                for (int k = 0; k < 128; ++k)
+                    q[k] = dg_ref_e4m3_from_float(bf16_bits_to_float(x[k]) * factor);
+                sa[((size_t)z * kb + g) * ld_sa + m] = scale;
+            }
         }
     }
 }

@@ -362,9 +362,73 @@ def check_grouped_masked(orc, seed=23):
     assert (p["masked_m"] < max_m).all()
 
 
+# ------------------------------------------------- activation quantiser --
+def _torch_e4m3_bits(v):
+    """torch's float32 -> float8_e4m3fn cast of v clamped to +-448 (its cast
+    does not saturate), as code bytes."""
+    t = torch.from_numpy(np.asarray(v, np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def check_e4m3_encode_vs_torch(orc, seed=29):
+    """The oracle's fp32 -> e4m3 rounding against torch's on every code value,
+    every midpoint between neighbouring values (the ties), values past the
+    largest finite one, the subnormal range and random magnitudes."""
+    vals = torch_e4m3_values()
+    fin = np.unique(vals[np.isfinite(vals)])
+    mids = (fin[:-1] + fin[1:]) / 2                  # exact in fp32
+    rng = np.random.default_rng(seed)
+    rnd = rng.standard_normal(3000) * np.exp2(rng.integers(-14, 10, 3000))
+    extra = [448.0, 449.0, 463.9, 464.0, 465.0, 1e6, -1e6, 2.0 ** -6, 2.0 ** -9, 2.0 ** -10,
+             3 * 2.0 ** -10, -(2.0 ** -10), 0.0, -0.0]
+    v = np.concatenate([fin, mids, rnd, extra]).astype(np.float32)
+    want = _torch_e4m3_bits(v)
+    got = np.array([orc.e4m3_from_float(x) for x in v], np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (v[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def check_quantize_invariants(orc, seed=31):
+    """Properties any correct 1x128 quantiser of this reading has, checked per
+    (row, group) on bf16 inputs spread over 40 binades: scale * 448 recovers
+    max(amax, 1e-4); the group maximum maps to code magnitude 448; every code
+    is x / scale rounded to the nearest e4m3 value (within half a step, signs
+    kept); zero and below-floor groups; scale columns past M untouched."""
+    rng = np.random.default_rng(seed)
+    G, M, K = 2, 5, 512
+    x = rng.standard_normal((G, M, K))
+    x *= np.repeat(np.exp2(rng.integers(-20, 20, (G, M, K // 128))), 128, axis=-1)
+    x[0, 1, 128:256] = 0.0                        # an all-zero group
+    x[1, 2, :128] = 1e-6 * np.sign(x[1, 2, :128])   # below the 1e-4 floor
+    xb = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    xf = xb.to(torch.float64).numpy()            # the exact bf16 values
+    Q, sa = orc.quantize_1x128(bits, ld_sa=8)
+    assert Q.shape == (G, M, K) and sa.shape == (G, K // 128, 8)
+    assert np.all(np.isnan(sa[:, :, M:])), "scale columns past M written"
+    dec = torch_e4m3_values()[Q.astype(np.int64)]
+    for z in range(G):
+        for m in range(M):
+            for g in range(K // 128):
+                blk = xf[z, m, g * 128:(g + 1) * 128]
+                d = dec[z, m, g * 128:(g + 1) * 128]
+                s = float(sa[z, g, m])
+                amax = float(np.abs(blk).max())
+                a = max(amax, 1e-4)
+                assert abs(s * 448.0 - a) <= a * 2.0 ** -22, (z, m, g, s, amax)
+                if amax > 1e-4:
+                    assert np.abs(d).max() == 448.0, (z, m, g)
+                t = np.clip(blk / s, -448.0, 448.0)
+                half = np.maximum(np.abs(t) * 2.0 ** -4, 2.0 ** -10) * (1 + 2.0 ** -20)
+                assert np.all(np.abs(d - t) <= half), (z, m, g)
+                assert np.all(d * t >= 0), (z, m, g)   # no sign flips
+    assert np.all(Q[0, 1, 128:256] & 0x7F == 0)
+
+
 ALL_CHECKS = [
     check_e4m3_golden, check_e4m3_all_codes, check_bf16_golden, check_bf16_bruteforce,
     check_bf16_vs_torch_float32, check_gemm_bruteforce, check_gemm_exact_integers,
     check_gemm_identity, check_gemm_linearity_transpose, check_gemm_closed_form,
-    check_grouped_contiguous, check_grouped_masked,
+    check_grouped_contiguous, check_grouped_masked, check_e4m3_encode_vs_torch,
+    check_quantize_invariants,
 ]

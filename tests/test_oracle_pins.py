@@ -4,7 +4,8 @@ See tests/oracle_checks.py for what each check compares with.  The mutant test
 compiles the oracle again with one planted mistake at a time (a dropped K
 group, a transposed scale index, a flushed subnormal, truncation instead of
 round-to-nearest-even, a dropped sign, a transposed operand, a dropped scale,
-padding rows computed, the mask ignored) and shows that at least one check
+padding rows computed, the mask ignored, the quantiser's 448 left out,
+truncation in the e4m3 encoder) and shows that at least one check
 fails for each, so the checks are able to see such mistakes.
 """
 import pytest
@@ -35,6 +36,8 @@ MUTANTS = {
     8: "B scale dropped",
     9: "padding rows computed",
     10: "mask ignored",
+    11: "quantiser scale without 448",
+    12: "e4m3 encode truncates",
 }
 
 
