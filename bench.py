@@ -41,7 +41,7 @@ METRIC = "FP8 block-scaled GEMM TFLOPS & HBM GB/s, % of GB300 FP8/HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
-HBM_BOUND = ("dense_decode",)
+HBM_BOUND = ("dense_decode", "quantize_act")
 
 
 # ------------------------------------------------------------- workloads ---
@@ -53,6 +53,13 @@ class Case:
         self.p = prob
         self.label = label
         K = prob["K"]
+        if kind == "quantize":
+            # bf16 read, e4m3 written, one fp32 scale per 128 elements
+            M = prob["M"]
+            self.m_valid = M
+            self.flops = 0.0
+            self.bytes = 2 * M * K + M * K + 4 * M * (K // 128)
+            return
         kb = K // 128
         N = prob["N"]
         nb = (N + 127) // 128
@@ -71,7 +78,11 @@ class Case:
 def make_cases(name, only=None):
     cfg = W.CONFIGS[name]
     out = []
-    if cfg["kind"] == "dense":
+    if cfg["kind"] == "quantize":
+        for (M, K) in cfg["cases"]:
+            out.append(("quantize", lambda M=M, K=K: W.activation_problem(M, K, seed=cfg["seed"]),
+                        f"{M}x{K}"))
+    elif cfg["kind"] == "dense":
         for (M, N, K) in cfg["cases"]:
             out.append(("dense", lambda M=M, N=N, K=K: W.dense_problem(M, N, K, seed=cfg["seed"]),
                         f"{M}x{N}x{K}"))
@@ -99,6 +110,9 @@ def describe(name):
     if name == "dense_prefill":
         return "dense prefill sweep: M=4096 x (N,K) in " + ",".join(
             f"({n},{k})" for n, k in W.DENSE_NK)
+    if name == "quantize_act":
+        return ("per-token 1x128 FP8 quantisation of bf16 activations [M,K]: M in {64,128,4096} "
+                "x K in {512,1536,2048,7168,16384}")
     if name == "dense_tiny":
         return "dense M=128, N=256, K=512"
     if name == "grouped_contiguous":
@@ -106,6 +120,12 @@ def describe(name):
                 f"{cfg['m_range'][1]}] padded to 128, (N,K) in {cfg['nk']}")
     return (f"masked M-grouped: G in {cfg['groups']}, max_m={cfg['max_m']}, "
             f"masked_m~U[1,{2 * cfg['expected_m']}], (N,K) in {cfg['nk']}")
+
+
+def data_desc(name):
+    if name == "quantize_act":
+        return "synthetic (seeded N(0,1) bf16 activations)"
+    return "synthetic (seeded N(0,1), 1x128 / 128x128 fp32-scaled e4m3)"
 
 
 def measured_peaks():
@@ -218,6 +238,14 @@ class DeviceCase:
         self.dg = dg
         p = c.p
         dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()  # noqa: E731
+        if c.kind == "quantize":
+            self.X = dev(p["X"].view(np.int16))
+            self.D = torch.empty((p["M"], p["K"]), dtype=torch.uint8, device="cuda")   # codes
+            self.sa = torch.zeros((p["K"] // 128, p["ld_sa"]), dtype=torch.float32,
+                                  device="cuda")
+            self.idx = None
+            self.inputs = [self.X]
+            return
         self.A, self.sa, self.B, self.sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])
         self.idx = None
         if c.kind == "dense":
@@ -234,7 +262,9 @@ class DeviceCase:
 
     def call(self, stream):
         p, dg = self.c.p, self.dg
-        if self.c.kind == "dense":
+        if self.c.kind == "quantize":
+            dg.quantize_fp8_1x128(self.X, self.D, self.sa, 1, p["M"], p["K"], p["ld_sa"], stream)
+        elif self.c.kind == "dense":
             dg.gemm_fp8_fp8_bf16_nt(self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D,
                                     p["M"], p["N"], p["K"], stream)
         elif self.c.kind == "contiguous":
@@ -377,8 +407,9 @@ def run_ours(args):
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic (seeded N(0,1), 1x128 / 128x128 fp32-scaled e4m3)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if args.workload == "quantize_act" else "e4m3",
+        "data": data_desc(args.workload),
         "config": {"workload": desc, "cases": len(cases),
                    "launch": "one CUDA graph per step (all cases), inputs resident in HBM",
                    "l2": (f"inputs larger than L2: step footprint {footprint / 1e6:.0f} MB vs "
@@ -470,6 +501,12 @@ def _oracle_sample(orc, c, rows, ncols, threads):
     of case c.  Returns (seconds, sampled output elements, output elements of
     the whole case)."""
     p = c.p
+    if c.kind == "quantize":
+        # `rows` whole rows (the quantiser has no output columns to sample)
+        r = np.linspace(0, p["M"] - 1, num=min(rows, p["M"])).astype(np.int64)
+        t = time.perf_counter()
+        orc.quantize_1x128(p["X"][r], nthreads=threads)
+        return time.perf_counter() - t, r.size * p["K"], p["M"] * p["K"]
     ncols = min(ncols, p["N"])
     nbs = (ncols + 127) // 128
     if c.kind == "dense":
@@ -509,7 +546,7 @@ def cpu_baseline(cases):
     cores = len(os.sched_getaffinity(0))
     t_full, wall, total_bytes = 0.0, 0.0, 0
     for c in cases:
-        secs, done, full = _oracle_sample(orc, c, cores, c.p["N"], cores)
+        secs, done, full = _oracle_sample(orc, c, cores, c.p.get("N", 0), cores)
         wall += secs
         t_full += secs * full / done
         total_bytes += c.bytes
@@ -535,13 +572,19 @@ def run_reference(args):
     warm = args.warmup
     budget = 120.0 / max(1, steps + warm)
     s, done, _ = _oracle_sample(orc, cases[0], cores, 128, cores)
-    rate = done * cases[0].p["K"] / max(s, 1e-6)  # output-element MACs per second
+    quant = cases[0].kind == "quantize"
+    # output-element MACs (quantiser: elements) per second
+    rate = done * (1 if quant else cases[0].p["K"]) / max(s, 1e-6)
     t_full, bytes_sum, wall = 0.0, 0, 0.0
     for i in range(warm + steps):
         c = cases[i % len(cases)]
-        rows = min(cores, c.m_valid)
-        cols = int(budget * rate / (rows * c.p["K"]))
-        cols = max(16, min(c.p["N"], cols // 16 * 16))
+        if quant:
+            rows = max(1, min(c.m_valid, int(budget * rate / c.p["K"])))
+            cols = 0
+        else:
+            rows = min(cores, c.m_valid)
+            cols = int(budget * rate / (rows * c.p["K"]))
+            cols = max(16, min(c.p["N"], cols // 16 * 16))
         secs, done, full = _oracle_sample(orc, c, rows, cols, cores)
         if i >= warm:
             wall += secs
@@ -555,8 +598,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": round(wall / steps * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1), 1x128 / 128x128 fp32-scaled e4m3)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if args.workload == "quantize_act" else "f64",
+        "data": data_desc(args.workload),
         "config": {"workload": describe(args.workload), "cases": len(cases),
                    "parallelism": "host cores (OpenMP over output rows)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,

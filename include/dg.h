@@ -95,6 +95,31 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
                                                    int max_m, int N, int K, int expected_m,
                                                    void* stream);
 
+/* Per-token 1x128 FP8 quantisation of a bf16 activation matrix: the step that
+ * produces the left operand A and its scales sa in the layout the GEMMs above
+ * read (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
+ * layout": LHS scales fp32, transposed and TMA-aligned; the pages leave the
+ * conversion itself to the caller, so its arithmetic is this library's
+ * reading).  For each row m and 128-wide K group g, in fp32:
+ *   a = max(max_k |X[m,k]|, 1e-4);  sa[g][m] = a / 448;
+ *   Q[m,k] = e4m3(X[m,k] * (448 / a)), rounded to nearest even, saturating
+ *   at +-448 (so the group's largest |X| becomes code magnitude 448).
+ *   X   bf16 [num_groups][M][K] row-major (num_groups = 1 for a dense matrix,
+ *       or G for the masked layout [G][max_m][K] with M = max_m); finite values
+ *   Q   e4m3 codes, same shape as X
+ *   sa  fp32 [num_groups][K/128][ld_sa]; columns m < M are written, the
+ *       others (ld_sa - M of them per row) are left as they were
+ * Requirements (checked on the host; on failure nothing is launched):
+ * non-null pointers, num_groups >= 1, M >= 0, ld_sa >= M (else
+ * DG_ERR_INVALID_ARG); K a positive multiple of 128, num_groups * M * K/128
+ * < 2^31, K/128 <= 65535 and num_groups <= 65535 (else
+ * DG_ERR_UNSUPPORTED_SHAPE); ld_sa a multiple of 4 and X, Q, sa
+ * 16-byte aligned (else DG_ERR_MISALIGNED).  M = 0 does nothing.
+ * Asynchronous on `stream`; device memory is caller-owned; no allocation, no
+ * host synchronisation. */
+dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
+                                int ld_sa, void* stream);
+
 /* Maximum number of SMs the kernels may use (DeepGEMM set_num_sms / get_num_sms,
  * es.news.hada.io/topic?id=19459, "Utilidades y variables de entorno").
  * dg_set_num_sms(0) restores "all SMs of the device"; a value above the device's

@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
-    "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "get_num_sms", "set_num_sms",
+    "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
     "plan_config", "num_output_tiles", "set_wait_timeout_ns", "debug_set_skip_producer",
     "debug_force_config", "debug_force_pair", "STATUS_NAMES", "EXPORTED_SYMBOLS",
@@ -32,7 +32,8 @@ STATUS_NAMES = {
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = [
     "dg_gemm_fp8_fp8_bf16_nt", "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
-    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_get_num_sms", "dg_set_num_sms",
+    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
+    "dg_set_num_sms",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_num_output_tiles",
     "dg_set_wait_timeout_ns", "dg_debug_set_skip_producer", "dg_debug_force_config",
@@ -71,6 +72,7 @@ def lib():
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+        L.dg_quantize_fp8_1x128.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_get_num_sms.argtypes = []
         L.dg_set_num_sms.argtypes = [_i]
         L.dg_get_tma_aligned_size.argtypes = [_i, _i]
@@ -137,6 +139,13 @@ def m_grouped_gemm_fp8_fp8_bf16_nt_masked(A, sa, ld_sa, B, sb, D, masked_m, num_
     _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(
         _ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D), _ptr(masked_m), num_groups, max_m,
         N, K, expected_m, _stream(stream)))
+
+
+def quantize_fp8_1x128(X, Q, sa, num_groups, M, K, ld_sa, stream=None):
+    """Per-token 1x128 FP8 quantisation of bf16 X [G,M,K] into e4m3 Q and fp32
+    sa [G,K/128,ld_sa]; see dg_quantize_fp8_1x128."""
+    _check(lib().dg_quantize_fp8_1x128(_ptr(X), _ptr(Q), _ptr(sa), num_groups, M, K, ld_sa,
+                                       _stream(stream)))
 
 
 def get_num_sms():

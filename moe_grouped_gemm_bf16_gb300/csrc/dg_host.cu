@@ -19,6 +19,7 @@
 
 #include "dg.h"
 #include "dg_instances.cuh"
+#include "dg_quant.h"
 
 // The device status word: kernels record the first device-side error here.
 __device__ unsigned int g_dg_status = 0;
@@ -500,6 +501,36 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
                                                    void* stream) {
   return run(dgk::kMasked, A, sa, ld_sa, B, sb, D, masked_m, max_m, N, K, num_groups, expected_m,
              stream);
+}
+
+dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
+                                int ld_sa, void* stream) {
+  read_env_once();
+  if (!X || !Q || !sa) return fail(DG_ERR_INVALID_ARG, "dg_quantize_fp8_1x128: null pointer");
+  if (num_groups < 1 || M < 0 || ld_sa < M)
+    return fail(DG_ERR_INVALID_ARG, "dg_quantize_fp8_1x128: G=%d M=%d ld_sa=%d", num_groups, M,
+                ld_sa);
+  if (K < 128 || K % 128 != 0)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "dg_quantize_fp8_1x128: K=%d (a positive multiple of 128)",
+                K);
+  if ((long long)num_groups * M * (K / 128) >= (1LL << 31) || K / 128 > 65535 ||
+      num_groups > 65535)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE,
+                "dg_quantize_fp8_1x128: needs num_groups * M * K/128 < 2^31, K/128 and "
+                "num_groups <= 65535");
+  if (ld_sa % 4 != 0 || !aligned16(X) || !aligned16(Q) || !aligned16(sa))
+    return fail(DG_ERR_MISALIGNED,
+                "dg_quantize_fp8_1x128: ld_sa a multiple of 4; X, Q, sa 16-byte aligned");
+  if (M == 0) return ok();  // nothing to do
+  DeviceState* st = nullptr;
+  int dev = 0;
+  dg_status s = device_state(&st, &dev);
+  if (s != DG_OK) return s;
+  const cudaError_t e = dgk::launch_quantize_1x128(X, Q, sa, num_groups, M, K, ld_sa,
+                                                   sms_in_use(*st),
+                                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+  return ok();
 }
 
 int dg_get_num_sms(void) {

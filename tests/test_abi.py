@@ -92,6 +92,31 @@ def test_grouped_argument_errors(L):
     assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked, **{**m, "max_m": 0}) == 0
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(X=None), 1),
+    (dict(sa=None), 1),
+    (dict(num_groups=0), 1),
+    (dict(M=-1), 1),
+    (dict(ld_sa=64), 1),
+    (dict(K=200), 2),
+    (dict(K=0), 2),
+    (dict(num_groups=1 << 12, M=1 << 12, K=128 * 256, ld_sa=1 << 12), 2),
+    (dict(ld_sa=130), 3),
+    (dict(X=P + 8), 3),
+    (dict(Q=P + 4), 3),
+])
+def test_quantiser_argument_errors(L, kw, code):
+    a = dict(X=P, Q=P, sa=P, num_groups=1, M=128, K=512, ld_sa=128)
+    a.update(kw)
+    assert status_of(dg.quantize_fp8_1x128, **a) == code
+    assert dg.lib().dg_last_error_string().decode() != ""
+
+
+def test_quantiser_empty_is_a_noop(L):
+    assert status_of(dg.quantize_fp8_1x128, X=P, Q=P, sa=P, num_groups=1, M=0, K=512,
+                     ld_sa=0) == 0
+
+
 def test_valid_call_without_device_reports_no_device(L):
     import torch
     if torch.cuda.is_available():

@@ -150,6 +150,15 @@ def random_codes(shape, seed, lo=0, hi=256, exclude_nan=True):
     return c
 
 
+def activation_problem(M, K, seed):
+    """A bf16 activation matrix [M,K] (N(0,1), as bit patterns) for the 1x128
+    quantiser, and the TMA-aligned leading dimension of its scales."""
+    g = _gen(seed)
+    x = torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return dict(X=x.view(torch.int16).numpy().view(np.uint16), M=M, K=K,
+                ld_sa=tma_aligned_ld(M))
+
+
 BF16_SENTINEL = 0xFFFF  # a NaN pattern no computed output can take
 
 #: Named workloads (shapes as the pages' DeepSeek-V3/R1 inference sweep).
@@ -162,4 +171,8 @@ CONFIGS = {
                                nk=GROUPED_NK, seed=1003),
     "grouped_masked": dict(kind="masked", groups=(1, 2, 4, 8), max_m=1024, expected_m=256,
                            nk=GROUPED_NK, seed=1004),
+    # the activations feeding the dense sweeps: A [M, K] for every M and K above
+    "quantize_act": dict(kind="quantize",
+                         cases=[(m, k) for m in (64, 128, 4096) for k in
+                                sorted({k for _, k in DENSE_NK})], seed=1005),
 }
