@@ -139,10 +139,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(workload):
+    """Hash of the sources a workload's kernels and launch choices come from:
+    the quantiser's own files for quantize_act, every other file for the
+    GEMM workloads (the host code, which plans and launches both, in each)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_grouped_gemm_bf16_gb300", "csrc")
+    quant = workload == "quantize_act"
     for f in sorted(os.listdir(csrc)):
+        if f != "dg_host.cu" and f.startswith("dg_quant") != quant:
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -162,7 +168,7 @@ def recorded_traffic(workload):
                     continue
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_hash") == kernel_source_hash():
+        if kv.get("kernel_hash") == kernel_source_hash(workload):
             return float(kv["dram_bytes_per_launch"])
     except Exception:
         pass
