@@ -25,6 +25,9 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
                    identity, linearity/transpose, float64 library closed form
   grouped_*        pinned: equal to per-expert / per-group dense runs,
                    padding rows +0 and masked rows untouched (bit-exact)
+  gemm_nt_c        pinned: C = 0 gives gemm_nt; zero A gives C back bit for
+                   bit; integer-valued C plus an exact integer GEMM gives the
+                   exact integer sum
   e4m3_from_float  pinned: torch's float32 -> float8_e4m3fn cast (after
                    clamping to +-448) on every code value, every midpoint
                    between neighbours (ties), saturation and random values
@@ -66,12 +69,14 @@ def _load(path):
                                                    _u16p, _int, _int, _int, _i64p, _int, _int]
     lib.dg_ref_grouped_masked.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _i32p, _u16p,
                                           _int, _int, _int, _int, _int]
+    lib.dg_ref_gemm_nt_c.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _u16p, _u16p, _int, _int,
+                                     _int, _int]
     lib.dg_ref_e4m3_from_float.argtypes = [ctypes.c_float]
     lib.dg_ref_e4m3_from_float.restype = ctypes.c_uint8
     lib.dg_ref_quantize_1x128.argtypes = [_u16p, _u8p, _f32p, _int, _int, _int, _int, _int]
     for f in ("dg_ref_gemm_nt_f64", "dg_ref_gemm_nt", "dg_ref_gemm_nt_rows",
               "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked",
-              "dg_ref_quantize_1x128"):
+              "dg_ref_quantize_1x128", "dg_ref_gemm_nt_c"):
         getattr(lib, f).restype = None
     return lib
 
@@ -134,6 +139,19 @@ class Oracle:
         D = np.zeros((M, N), np.uint16)
         self.lib.dg_ref_gemm_nt(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
                                 _p(sb, _f32p), _p(D, _u16p), M, N, K, nthreads)
+        return D
+
+    def gemm_nt_c(self, A, sa, B, sb, C, nthreads=0):
+        """D = bf16(C + sum_g ...): C bf16 bit patterns [M, N]."""
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32); C = _c(C, np.uint16)
+        M, K = A.shape
+        N = B.shape[0]
+        _check_dense(A, sa, B, sb)
+        assert C.shape == (M, N)
+        D = np.zeros((M, N), np.uint16)
+        self.lib.dg_ref_gemm_nt_c(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                  _p(sb, _f32p), _p(C, _u16p), _p(D, _u16p), M, N, K, nthreads)
         return D
 
     def gemm_nt_rows(self, A, sa, B, sb, rows, nthreads=0):

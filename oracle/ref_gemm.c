@@ -245,6 +245,35 @@ void dg_ref_gemm_nt(const uint8_t *A, const float *sa, int ld_sa,
     }
 }
 
+/* ------------------------------------------------- with an addend C ----- */
+/* D = C + A @ B^T (the GEMM naming convention of DeepGEMM,
+ * es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de layout"),
+ * here with C and D bf16 [M][N]: the bf16 C value, exact in double, is added
+ * to the unrounded double sum, and the total is rounded once to bf16. */
+void dg_ref_gemm_nt_c(const uint8_t *A, const float *sa, int ld_sa,
+                      const uint8_t *B, const float *sb, const uint16_t *C,
+                      uint16_t *D, int M, int N, int K, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; ++m) {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+        ref_row_f64(A + (size_t)m * K, sa, ld_sa, m, B, sb, N, K, acc);
+        for (int n = 0; n < N; ++n) {
+            uint32_t u = (uint32_t)C[(size_t)m * N + n] << 16;
+            float c;
+            memcpy(&c, &u, 4);
+#if DG_REF_MUTANT == 13
+            (void)c;
+            D[(size_t)m * N + n] = dg_ref_bf16_rne(acc[n]);   /* mutant: C dropped */
+#else
+            D[(size_t)m * N + n] = dg_ref_bf16_rne((double)c + acc[n]);
+#endif
+        }
+        free(acc);
+    }
+}
+
 /* ------------------------------------------------- grouped, contiguous --- */
 /* A: [M_total][K]; B: [G][N][K]; sa: [kb][ld_sa]; sb: [G][nb][kb];
  * m_indices: [M_total], expert of each row or -1 (padding -> +0).

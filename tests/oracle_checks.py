@@ -362,6 +362,37 @@ def check_grouped_masked(orc, seed=23):
     assert (p["masked_m"] < max_m).all()
 
 
+# --------------------------------------------------- D = C + A @ B^T -----
+def check_gemm_with_c(orc, seed=37):
+    """The addend form against independent results: C = 0 gives the plain
+    product; all-zero A gives C back bit for bit; integer-valued C (|C| < 64)
+    plus a sparse integer GEMM (|sum| < 64, unit scales) gives the exact
+    integer C + sum, which bf16 holds."""
+    ints = _int_codes()
+    rng = np.random.default_rng(seed)
+    p = W.dense_problem(7, 136, 384, seed)
+    zero = np.zeros((7, 136), np.uint16)
+    assert np.array_equal(orc.gemm_nt_c(p["A"], p["sa"], p["B"], p["sb"], zero),
+                          orc.gemm_nt(p["A"], p["sa"], p["B"], p["sb"]))
+    C = torch.from_numpy(rng.standard_normal((7, 136)).astype(np.float32)).to(torch.bfloat16)
+    Cb = C.view(torch.int16).numpy().view(np.uint16)
+    A0 = np.zeros_like(p["A"])
+    assert np.array_equal(orc.gemm_nt_c(A0, p["sa"], p["B"], p["sb"], Cb), Cb)
+    M, N, K = 6, 140, 256
+    av = np.where(rng.random((M, K)) < 0.03, rng.integers(-2, 3, (M, K)), 0)
+    bv = np.where(rng.random((N, K)) < 0.03, rng.integers(-2, 3, (N, K)), 0)
+    A = np.vectorize(ints.get)(av).astype(np.uint8)
+    B = np.vectorize(ints.get)(bv).astype(np.uint8)
+    sa = np.ones((K // 128, W.tma_aligned_ld(M)), np.float32)
+    sb = np.ones(((N + 127) // 128, K // 128), np.float32)
+    c_int = rng.integers(-40, 41, (M, N))
+    Cb = torch.from_numpy(c_int.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    exact = c_int + av.astype(np.int64) @ bv.astype(np.int64).T
+    assert np.abs(exact).max() < 256
+    want = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.gemm_nt_c(A, sa, B, sb, Cb), want)
+
+
 # ------------------------------------------------- activation quantiser --
 def _torch_e4m3_bits(v):
     """torch's float32 -> float8_e4m3fn cast of v clamped to +-448 (its cast
@@ -430,5 +461,5 @@ ALL_CHECKS = [
     check_bf16_vs_torch_float32, check_gemm_bruteforce, check_gemm_exact_integers,
     check_gemm_identity, check_gemm_linearity_transpose, check_gemm_closed_form,
     check_grouped_contiguous, check_grouped_masked, check_e4m3_encode_vs_torch,
-    check_quantize_invariants,
+    check_quantize_invariants, check_gemm_with_c,
 ]
