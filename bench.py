@@ -75,7 +75,7 @@ class Case:
         self.bytes = mv * K + gu * N * K + 4 * mv * kb + 4 * gu * nb * kb + 2 * mv * N
 
 
-def make_cases(name, only=None):
+def make_cases(name, only=None, add_c=False):
     cfg = W.CONFIGS[name]
     out = []
     if cfg["kind"] == "quantize":
@@ -99,7 +99,17 @@ def make_cases(name, only=None):
                     f"G{G}x{cfg['max_m']}x{N}x{K}"))
     if only is not None:
         out = [out[only]]
-    return [Case(kind, make(), label) for kind, make, label in out]
+    cases = [Case(kind, make(), label) for kind, make, label in out]
+    if add_c:
+        assert cfg["kind"] == "dense", "--add-c is for the dense workloads"
+        for c in cases:
+            M, N = c.p["M"], c.p["N"]
+            g = np.random.default_rng(c.p["K"] + M + N)
+            c.p["C"] = (g.standard_normal((M, N)).astype(np.float32).view(np.uint32) >>
+                        16).astype(np.uint16)   # bf16 bits (truncated N(0,1))
+            c.bytes += 2 * M * N
+            c.label += "+C"
+    return cases
 
 
 def describe(name):
@@ -254,6 +264,7 @@ class DeviceCase:
             return
         self.A, self.sa, self.B, self.sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])
         self.idx = None
+        self.C = dev(p["C"].view(np.int16)) if "C" in p else None
         if c.kind == "dense":
             self.D = torch.zeros((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda")
         elif c.kind == "contiguous":
@@ -264,12 +275,15 @@ class DeviceCase:
             self.D = torch.zeros((p["G"], p["max_m"], p["N"]), dtype=torch.bfloat16,
                                  device="cuda")
         self.inputs = [self.A, self.sa, self.B, self.sb] + (
-            [self.idx] if self.idx is not None else [])
+            [self.idx] if self.idx is not None else []) + ([self.C] if self.C is not None else [])
 
     def call(self, stream):
         p, dg = self.c.p, self.dg
         if self.c.kind == "quantize":
             dg.quantize_fp8_1x128(self.X, self.D, self.sa, 1, p["M"], p["K"], p["ld_sa"], stream)
+        elif self.c.kind == "dense" and self.C is not None:
+            dg.gemm_fp8_fp8_bf16_nt_add_c(self.A, self.sa, self.sa.shape[-1], self.B, self.sb,
+                                          self.C, self.D, p["M"], p["N"], p["K"], stream)
         elif self.c.kind == "dense":
             dg.gemm_fp8_fp8_bf16_nt(self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D,
                                     p["M"], p["N"], p["K"], stream)
@@ -320,7 +334,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     _build.build()
     dg.lib()
-    cases = make_cases(args.workload, args.case)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c)
     dcs = [DeviceCase(c, torch, dg) for c in cases]
     stream = torch.cuda.Stream()
     step_bytes = sum(c.bytes for c in cases)
@@ -407,6 +421,8 @@ def run_ours(args):
                 "traffic": recorded_traffic(args.workload),
                 "peak_source": (f"{src} bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)")}
     desc = describe(args.workload)
+    if args.add_c:
+        desc += "; D = C + A B^T with a bf16 addend C read per call"
     if args.case is not None:
         desc += f" (case {args.case} only: {cases[0].label})"
     big = footprint > 2 * L2_BYTES
@@ -573,7 +589,7 @@ def run_reference(args):
     import oracle
     orc = oracle.Oracle()
     cores = len(os.sched_getaffinity(0))
-    cases = make_cases(args.workload, args.case)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c)
     steps = args.steps if args.steps is not None else 2 * len(cases)
     warm = args.warmup
     budget = 120.0 / max(1, steps + warm)
@@ -629,6 +645,9 @@ def main(argv=None):
                     help="run only case I of the workload (profiling one shape)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--add-c", action="store_true",
+                    help="dense workloads: D = C + A B^T through dg_gemm_fp8_fp8_bf16_nt_add_c "
+                         "(a seeded bf16 addend C; its 2*M*N bytes count as read)")
     ap.add_argument("--quick", action="store_true",
                     help="skip the per-case cold-L2 detail (profiling runs)")
     args = ap.parse_args(argv)

@@ -66,6 +66,18 @@ typedef enum dg_status {
 dg_status dg_gemm_fp8_fp8_bf16_nt(const void* A, const float* sa, int ld_sa, const void* B,
                                   const float* sb, void* D, int M, int N, int K, void* stream);
 
+/* The same dense GEMM with an addend: D = C + A @ B^T (the naming convention
+ * D = C + A @ B of es.news.hada.io/topic?id=19459, "Interfaz GEMM y
+ * restricciones de layout").  C is bf16 [M][N] row-major, 16-byte aligned,
+ * caller-owned; it may be D itself (each element is read before it is
+ * written, by the same thread).  Per element, the C value is added in fp32 to
+ * the fp32 sum of the scaled K groups, and the total is rounded once to bf16.
+ * Everything else, errors included, is as for dg_gemm_fp8_fp8_bf16_nt; a null
+ * C is DG_ERR_INVALID_ARG. */
+dg_status dg_gemm_fp8_fp8_bf16_nt_add_c(const void* A, const float* sa, int ld_sa, const void* B,
+                                        const float* sb, const void* C, void* D, int M, int N,
+                                        int K, void* stream);
+
 /* M-grouped GEMM, contiguous layout (DeepGEMM "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous";
  * es.news.hada.io/topic?id=19459, "Dense y Grouped GEMM": the experts' rows are
  * concatenated along M, each expert's segment aligned to the M block size).

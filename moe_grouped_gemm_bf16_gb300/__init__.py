@@ -13,7 +13,8 @@ import ctypes
 import os
 
 __all__ = [
-    "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
+    "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "gemm_fp8_fp8_bf16_nt_add_c",
+    "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
     "plan_config", "num_output_tiles", "set_wait_timeout_ns", "debug_set_skip_producer",
@@ -31,7 +32,8 @@ STATUS_NAMES = {
 
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = [
-    "dg_gemm_fp8_fp8_bf16_nt", "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
+    "dg_gemm_fp8_fp8_bf16_nt", "dg_gemm_fp8_fp8_bf16_nt_add_c",
+    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
     "dg_set_num_sms",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
@@ -68,6 +70,8 @@ def lib():
                                "`python -m moe_grouped_gemm_bf16_gb300._build`")
         L = ctypes.CDLL(LIB_PATH)
         L.dg_gemm_fp8_fp8_bf16_nt.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]
+        L.dg_gemm_fp8_fp8_bf16_nt_add_c.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                                    _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked.argtypes = [
@@ -125,6 +129,12 @@ def gemm_fp8_fp8_bf16_nt(A, sa, ld_sa, B, sb, D, M, N, K, stream=None):
     """D[M,N] = bf16(sum_g (A_g B_g^T) sa sb); see dg_gemm_fp8_fp8_bf16_nt."""
     _check(lib().dg_gemm_fp8_fp8_bf16_nt(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D),
                                          M, N, K, _stream(stream)))
+
+
+def gemm_fp8_fp8_bf16_nt_add_c(A, sa, ld_sa, B, sb, C, D, M, N, K, stream=None):
+    """D[M,N] = bf16(C + sum_g (A_g B_g^T) sa sb); C may be D."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_nt_add_c(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb),
+                                               _ptr(C), _ptr(D), M, N, K, _stream(stream)))
 
 
 def m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(A, sa, ld_sa, B, sb, D, m_indices, M_total, N, K,

@@ -332,7 +332,8 @@ dg_status encode(CUtensorMap* m, CUtensorMapDataType dt, void* ptr, const uint64
 
 // A [z][rows][K] e4m3, B [g][N][K] e4m3, sa [z][kb][ld_sa] fp32, D [z][rows][N] bf16.
 dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, const void* B,
-                    void* D, int rows, int zA, int N, int K, int gB, int block_n, int a_rows) {
+                    void* D, int rows, int zA, int N, int K, int gB, int block_n, int a_rows,
+                    const void* C = nullptr) {
   const int kb = K / 128;
   {
     const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)zA};
@@ -366,6 +367,14 @@ dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, co
     dg_status s = encode(&mp->d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, dims, str, box,
                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
     if (s != DG_OK) return s;
+    // the addend C: loaded into the staging tile in exactly the store's layout
+    if (C) {
+      s = encode(&mp->c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(C), dims, str, box,
+                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "C");
+      if (s != DG_OK) return s;
+    } else {
+      std::memset(&mp->c, 0, sizeof(mp->c));
+    }
   }
   return DG_OK;
 }
@@ -384,7 +393,7 @@ const char* kind_name(int kind) {
 // (contiguous) or max_m (masked); idx = m_indices or masked_m.
 dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B, const float* sb,
               void* D, const int32_t* idx, int rows, int N, int K, int G, int expected_m,
-              void* stream) {
+              void* stream, const void* C = nullptr) {
   read_env_once();
   // -------- validation (host only; nothing is launched on an error) ------
   if (rows < 0 || N < 0 || K < 0)
@@ -403,9 +412,9 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
     return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
   if (kind != dgk::kDense && !idx)
     return fail(DG_ERR_INVALID_ARG, "null %s", kind == dgk::kMasked ? "masked_m" : "m_indices");
-  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sa) ||
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sa) || (C && !aligned16(C)) ||
       (reinterpret_cast<uintptr_t>(sb) & 3u) || (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
-    return fail(DG_ERR_MISALIGNED, "A, B, D and sa need 16-byte alignment, sb and indices 4");
+    return fail(DG_ERR_MISALIGNED, "A, B, C, D and sa need 16-byte alignment, sb and indices 4");
   if (ld_sa < rows || ld_sa % 4 != 0 || ld_sa < 1)
     return fail(ld_sa % 4 != 0 ? DG_ERR_MISALIGNED : DG_ERR_INVALID_ARG,
                 "ld_sa=%d: need >= %d and a multiple of 4", ld_sa, rows);
@@ -438,7 +447,8 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
 
   dgk::Maps maps;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
-                kind == dgk::kDense ? 1 : G, in.pair ? in.block_n / 2 : in.block_n, in.a_rows);
+                kind == dgk::kDense ? 1 : G, in.pair ? in.block_n / 2 : in.block_n, in.a_rows,
+                kind == dgk::kDense ? C : nullptr);
   if (s != DG_OK) return s;
 
   dgk::Params p{};
@@ -456,6 +466,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
   p.masked_m = kind == dgk::kMasked ? idx : nullptr;
   p.D = static_cast<uint16_t*>(D);
+  p.C = static_cast<const uint16_t*>(C);
   p.status = st->status;
   p.timeout_ns = g_timeout_ns.load();
   p.debug_flags = g_skip_producer.load() ? dgk::DBG_SKIP_PRODUCER : 0u;
@@ -483,6 +494,13 @@ extern "C" {
 dg_status dg_gemm_fp8_fp8_bf16_nt(const void* A, const float* sa, int ld_sa, const void* B,
                                   const float* sb, void* D, int M, int N, int K, void* stream) {
   return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_nt_add_c(const void* A, const float* sa, int ld_sa, const void* B,
+                                        const float* sb, const void* C, void* D, int M, int N,
+                                        int K, void* stream) {
+  if (!C) return fail(DG_ERR_INVALID_ARG, "null addend C (use dg_gemm_fp8_fp8_bf16_nt)");
+  return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream, C);
 }
 
 dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(const void* A, const float* sa, int ld_sa,

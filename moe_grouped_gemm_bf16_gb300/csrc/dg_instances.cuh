@@ -10,7 +10,7 @@
 namespace dgk {
 
 struct Maps {
-  CUtensorMap a, b, sa, d;
+  CUtensorMap a, b, sa, d, c;  // c: the dense form's addend (unused when there is none)
 };
 
 struct Instance {
@@ -66,7 +66,7 @@ struct InstanceOf {
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.sa, m.d, p);
+    return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.sa, m.d, m.c, p);
   }
 
   static cudaError_t set_smem(int smem) {

@@ -62,7 +62,7 @@ struct SmemLayout {
   static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
                        T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
-                       MMA_DONE = READY + 1, NUM_BARS = MMA_DONE + 1;
+                       MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, NUM_BARS = C_FULL + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int DYN_OFF = MISC_OFF + 16;            // sb tile, then masked tables
   static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
@@ -198,7 +198,7 @@ template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PA
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
-                const Params p) {
+                const __grid_constant__ CUtensorMap tmC, const Params p) {
   static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
@@ -255,6 +255,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init(bar(L::RED_FULL), 1);
     mbar_init(bar(L::READY), S);
     mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
+    mbar_init(bar(L::C_FULL), 1);
     misc[1] = 0;
     fence_mbarrier_init();
   }
@@ -472,9 +473,28 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int b = 0, j = 0;
     uint32_t bph = 0, jph = 0;
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
+    uint32_t cph = 0;                   // phase of the addend's barrier
     float acc[HALF];
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
+      // Dense form with an addend (D = C + A B^T): thread 0 loads this tile's C
+      // into the staging tile, in the store's own layout, halfway through the
+      // tile's K groups (the previous tile's store has long finished reading
+      // the staging tile by then, and C has long landed by the epilogue).
+      const bool load_c = MODE == kDense && !SPLIT && p.C != nullptr && pt == 0;
+      const int g_c = (T.skip || kcnt == 0) ? -1 : kbeg + kcnt / 2;   // K group after which C loads
+      auto issue_c = [&]() {
+        bulk_wait_group_read0();
+        uint32_t bytes = 0;
+        for (int cc = 0; cc < BN / 32; ++cc)
+          if (T.n0 + cc * 32 < p.N) bytes += BLOCK_M * 64;
+        mbar_arrive_expect_tx(bar(L::C_FULL), bytes);
+        for (int cc = 0; cc < BN / 32; ++cc)
+          if (T.n0 + cc * 32 < p.N)
+            tma_load_3d(out_s + cc * (BLOCK_M * 64), &tmC, bar(L::C_FULL), T.n0 + cc * 32, T.m0,
+                        T.z);
+      };
+      if (load_c && g_c < 0) issue_c();
       // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
       if (!T.skip) {
@@ -549,6 +569,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
           }
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
+          if (load_c && g == g_c) issue_c();
         }
       }
       if constexpr (!SPLIT) {
@@ -566,6 +587,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
           }
         }
+        // dense form with an addend: wait for this tile's C in the staging tile
+        // (each thread reads exactly the 16-byte units it writes below)
+        bool c_in = false;
+        if constexpr (MODE == kDense) {
+          if (p.C != nullptr) {
+            c_in = wait_bar(bar(L::C_FULL), cph, abort_flag, p);
+            cph ^= 1;
+          }
+        }
         if (pt == 0) bulk_wait_group_read0();  // the previous store has read the staging tile
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         // staging: BN/32 chunks of [128 rows x 64 B], 64-byte swizzle (16-byte
@@ -577,12 +607,22 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int o = c * 32 + u * 8;
+            const uint32_t addr = rbase + ((u ^ ((row >> 1) & 3)) << 4);
+            if (c_in) {   // D = C + A B^T: the addend, added in fp32 before the rounding
+              const uint4 cv = ld_shared_v4(addr);
+              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[o + 2 * e] += __uint_as_float(cw[e] << 16);
+                acc[o + 2 * e + 1] += __uint_as_float(cw[e] & 0xFFFF0000u);
+              }
+            }
             uint32_t w0 = pack_bf16x2(acc[o + 0], acc[o + 1]);
             uint32_t w1 = pack_bf16x2(acc[o + 2], acc[o + 3]);
             uint32_t w2 = pack_bf16x2(acc[o + 4], acc[o + 5]);
             uint32_t w3 = pack_bf16x2(acc[o + 6], acc[o + 7]);
             if (zero_row) w0 = w1 = w2 = w3 = 0u;
-            st_shared_v4(rbase + ((u ^ ((row >> 1) & 3)) << 4), w0, w1, w2, w3);
+            st_shared_v4(addr, w0, w1, w2, w3);
           }
         }
         fence_proxy_async_smem();
@@ -658,7 +698,27 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const bool red_ok = wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
         __syncwarp();
         constexpr int UPR = BN / 4;  // 16-byte units per row
-        for (int i = pt; i < own_rows * UPR; i += 32 * NUM_PROMO_WARPS) {
+        // addend C (D = C + A B^T): this thread's C values for all its units
+        // are loaded before the sums, so their latencies overlap (an owner's
+        // slice has at most AROWS rows)
+        constexpr int MAX_IT = (AROWS * UPR + 32 * NUM_PROMO_WARPS - 1) / (32 * NUM_PROMO_WARPS);
+        uint2 cpre[MAX_IT];
+#pragma unroll
+        for (int it = 0; it < MAX_IT; ++it) {
+          const int i = pt + it * 32 * NUM_PROMO_WARPS;
+          cpre[it] = make_uint2(0, 0);
+          if (p.C != nullptr && i < own_rows * UPR) {
+            const int rr = i / UPR, cu = i - rr * UPR;
+            const int n = T.n0 + cu * 4;
+            if (n < p.N)
+              cpre[it] = __ldg(reinterpret_cast<const uint2*>(
+                  p.C + static_cast<size_t>(T.m0 + own_r0 + rr) * p.N + n));
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < MAX_IT; ++it) {
+          const int i = pt + it * 32 * NUM_PROMO_WARPS;
+          if (i >= own_rows * UPR) break;
           const int rr = i / UPR, cu = i - rr * UPR;
           const int grow = own_r0 + rr;  // row in the tile (its swizzle key)
           const uint32_t off = static_cast<uint32_t>(rr * ROWB + ((cu ^ (grow & 7)) << 4));
@@ -676,6 +736,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (r < S) {
               sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
             }
+          if (p.C != nullptr) {
+            sum.x += __uint_as_float(cpre[it].x << 16);
+            sum.y += __uint_as_float(cpre[it].x & 0xFFFF0000u);
+            sum.z += __uint_as_float(cpre[it].y << 16);
+            sum.w += __uint_as_float(cpre[it].y & 0xFFFF0000u);
+          }
           const int n = T.n0 + cu * 4;
           if (n < p.N && !*abort_flag) {
             uint2 w;

@@ -62,6 +62,7 @@ struct Params {
   const int32_t* m_indices;    // contiguous: [M_total]
   const int32_t* masked_m;     // masked: [G]
   uint16_t* D;                 // bf16 output, [M][N] or [G][max_m][N]
+  const uint16_t* C;           // dense only: bf16 addend [M][N] (D = C + A B^T), or null
   unsigned int* status;        // device status word
   unsigned long long timeout_ns;
   unsigned int debug_flags;

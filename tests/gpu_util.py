@@ -53,6 +53,18 @@ def to_bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def run_dense_add_c(p, C_bits, inplace=False):
+    """D = C + A B^T through dg_gemm_fp8_fp8_bf16_nt_add_c; with `inplace` the
+    addend buffer is the output."""
+    M, N, K = p["M"], p["N"], p["K"]
+    A, sa, B, sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])
+    C = dev(np.ascontiguousarray(C_bits).view(np.int16))
+    D = C if inplace else torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    dg.gemm_fp8_fp8_bf16_nt_add_c(A, sa, sa.shape[-1], B, sb, C, D, M, N, K)
+    torch.cuda.synchronize()
+    return to_bits(D)
+
+
 def run_dense(p, fill=W.BF16_SENTINEL):
     M, N, K = p["M"], p["N"], p["K"]
     A, sa, B, sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])

@@ -72,6 +72,12 @@ def test_dense_argument_errors(L, kw, code):
     assert dg.lib().dg_last_error_string().decode() != ""
 
 
+def test_add_c_requires_c(L):
+    a = _dense()
+    assert status_of(dg.gemm_fp8_fp8_bf16_nt_add_c, C=None, **a) == 1
+    assert status_of(dg.gemm_fp8_fp8_bf16_nt_add_c, C=P + 8, **a) == 3
+
+
 def test_empty_problem_is_a_noop(L):
     # M = 0: nothing to compute, no device needed
     assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(M=0)) == 0

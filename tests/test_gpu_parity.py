@@ -176,3 +176,75 @@ def test_dense_pair_off_matches():
     want = dense_ref(p)
     U.assert_close(a, want, "pair off")
     U.assert_close(b, want, "pair on")
+
+
+def test_dense_largest_k():
+    """K = 128 * 512, the largest the kernels take (the B-scale staging holds
+    three 128-column blocks for every K group)."""
+    p = W.dense_problem(64, 272, 128 * 512, seed=31)
+    got = U.run_dense(p)
+    U.assert_close(got, dense_ref(p), "K = 65536")
+
+
+def test_graph_replay_sees_new_inputs():
+    """The calls capture into a CUDA graph (no host synchronisation, no host
+    read of device data); replaying the graph after overwriting the inputs in
+    place computes on the new values."""
+    p1 = W.dense_problem(200, 384, 1024, seed=41)
+    p2 = W.dense_problem(200, 384, 1024, seed=42)
+    M, N, K = 200, 384, 1024
+    A, sa, B, sb = U.dev(p1["A"]), U.dev(p1["sa"]), U.dev(p1["B"]), U.dev(p1["sb"])
+    D = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dg.gemm_fp8_fp8_bf16_nt(A, sa, sa.shape[-1], B, sb, D, M, N, K, s.cuda_stream)  # warm-up
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dg.gemm_fp8_fp8_bf16_nt(A, sa, sa.shape[-1], B, sb, D, M, N, K, s.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    U.assert_close(U.to_bits(D), dense_ref(p1), "graph replay 1")
+    for dst, src in ((A, p2["A"]), (sa, p2["sa"]), (B, p2["B"]), (sb, p2["sb"])):
+        dst.copy_(torch.from_numpy(np.ascontiguousarray(src)))
+    g.replay()
+    torch.cuda.synchronize()
+    U.assert_close(U.to_bits(D), dense_ref(p2), "graph replay 2")
+    assert dg.get_device_status() == 0
+
+
+ADD_C_SHAPES = [(64, 144, 640), (200, 400, 384), (333, 2112, 256), (512, 528, 1024)]
+ADD_C_CFGS = [(0, 0, -1), (128, 1, 0), (256, 1, 0), (128, 3, 0), (256, 5, 0), (256, 1, 1),
+              (128, 1, 1)]
+
+
+def _addend(M, N, seed):
+    g = torch.Generator().manual_seed(seed)
+    c = torch.randn(M, N, generator=g) * 4.0
+    return c.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("shape", ADD_C_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("cfg", ADD_C_CFGS, ids=lambda c: f"bn{c[0]}_s{c[1]}_p{c[2]}")
+def test_dense_add_c(shape, cfg):
+    """D = C + A B^T in every dense form (plain, K split with full and 64-row
+    A, CTA pair) against the oracle's addend form."""
+    M, N, K = shape
+    p = W.dense_problem(M, N, K, seed=M + 2 * N + K)
+    C = _addend(M, N, seed=M * N)
+    with U.forced_config(cfg[0], cfg[1], pair=cfg[2]):
+        got = U.run_dense_add_c(p, C)
+    want = ORC.gemm_nt_c(p["A"], p["sa"], p["B"], p["sb"], C)
+    U.assert_close(got, want, f"add_c {shape} cfg={cfg}")
+
+
+@pytest.mark.parametrize("cfg", [(0, 0, -1), (128, 3, 0), (256, 1, 1)],
+                         ids=lambda c: f"bn{c[0]}_s{c[1]}_p{c[2]}")
+def test_dense_add_c_in_place(cfg):
+    """C is D: the output buffer accumulates."""
+    M, N, K = 130, 272, 512
+    p = W.dense_problem(M, N, K, seed=88)
+    C = _addend(M, N, seed=89)
+    with U.forced_config(cfg[0], cfg[1], pair=cfg[2]):
+        got = U.run_dense_add_c(p, C, inplace=True)
+    U.assert_close(got, ORC.gemm_nt_c(p["A"], p["sa"], p["B"], p["sb"], C), f"in place {cfg}")
