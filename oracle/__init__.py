@@ -28,6 +28,14 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   gemm_nt_c        pinned: C = 0 gives gemm_nt; zero A gives C back bit for
                    bit; integer-valued C plus an exact integer GEMM gives the
                    exact integer sum
+  gemm_layout      pinned: each of nn / tn / tt equals gemm_nt on the
+                   operands transposed by numpy (non-square, ragged N, so a
+                   swapped index fails); "nt" through it equals gemm_nt; C
+                   handled as in gemm_nt_c
+  k_grouped_tn     pinned: every group equals gemm_nt (or gemm_nt_c) on its
+                   own K slice transposed by numpy, with its own scale
+                   columns; an empty group gives C (or +0) bit for bit; one
+                   group over all of K equals gemm_layout "tn"
   e4m3_from_float  pinned: torch's float32 -> float8_e4m3fn cast (after
                    clamping to +-448) on every code value, every midpoint
                    between neighbours (ties), saturation and random values
@@ -73,6 +81,10 @@ def _load(path):
                                      _int, _int]
     lib.dg_ref_e4m3_from_float.argtypes = [ctypes.c_float]
     lib.dg_ref_e4m3_from_float.restype = ctypes.c_uint8
+    lib.dg_ref_gemm_layout.argtypes = [_u8p, _int, _f32p, _int, _u8p, _int, _f32p, _u16p, _u16p,
+                                       _int, _int, _int, _int]
+    lib.dg_ref_k_grouped_tn.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _u16p, _u16p, _int, _int,
+                                        _i32p, _int, _int]
     lib.dg_ref_quantize_1x128.argtypes = [_u16p, _u8p, _f32p, _int, _int, _int, _int, _int]
     for f in ("dg_ref_gemm_nt_f64", "dg_ref_gemm_nt", "dg_ref_gemm_nt_rows",
               "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked",
@@ -152,6 +164,56 @@ class Oracle:
         D = np.zeros((M, N), np.uint16)
         self.lib.dg_ref_gemm_nt_c(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
                                   _p(sb, _f32p), _p(C, _u16p), _p(D, _u16p), M, N, K, nthreads)
+        return D
+
+    def gemm_layout(self, layout, A, sa, B, sb, C=None, nthreads=0):
+        """D = bf16(C + A @ B) in storage layout `layout` ("nt", "nn", "tn" or
+        "tt"): A [M,K] for "n" or [K,M] for "t"; B [N,K] for "t" or [K,N] for
+        "n"; sa [kb, ld_sa]; sb [nb, kb]; C bf16 bits [M, N] or None."""
+        assert layout in ("nt", "nn", "tn", "tt")
+        a_t, b_n = layout[0] == "t", layout[1] == "n"
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        K, M = A.shape if a_t else A.shape[::-1]
+        N = B.shape[1] if b_n else B.shape[0]
+        assert (B.shape[0] if b_n else B.shape[1]) == K and K % 128 == 0
+        assert sa.ndim == 2 and sa.shape[0] == K // 128 and sa.shape[1] >= M
+        assert sb.shape == ((N + 127) // 128, K // 128)
+        D = np.zeros((M, N), np.uint16)
+        cp = None
+        if C is not None:
+            C = _c(C, np.uint16)
+            assert C.shape == (M, N)
+            cp = _p(C, _u16p)
+        self.lib.dg_ref_gemm_layout(_p(A, _u8p), int(a_t), _p(sa, _f32p), sa.shape[-1],
+                                    _p(B, _u8p), int(b_n), _p(sb, _f32p), cp, _p(D, _u16p),
+                                    M, N, K, nthreads)
+        return D
+
+    def k_grouped_tn(self, A, sa, B, sb, ks, C=None, nthreads=0):
+        """K-grouped D[g] = bf16(C[g] + A_g^T B_g): A [K_all, M], B [K_all, N],
+        ks the K rows of each group (multiples of 128, summing to K_all),
+        sa [K_all/128, ld_sa], sb [nb, K_all/128], C bf16 bits [G, M, N] or
+        None.  Returns D [G, M, N]."""
+        A = _c(A, np.uint8); B = _c(B, np.uint8)
+        sa = _c(sa, np.float32); sb = _c(sb, np.float32)
+        ks = _c(ks, np.int32)
+        K_all, M = A.shape
+        N = B.shape[1]
+        G = ks.shape[0]
+        assert B.shape[0] == K_all and int(ks.sum()) == K_all
+        assert np.all(ks % 128 == 0) and np.all(ks >= 0)
+        assert sa.ndim == 2 and sa.shape[0] == K_all // 128 and sa.shape[1] >= M
+        assert sb.shape == ((N + 127) // 128, K_all // 128)
+        D = np.zeros((G, M, N), np.uint16)
+        cp = None
+        if C is not None:
+            C = _c(C, np.uint16)
+            assert C.shape == (G, M, N)
+            cp = _p(C, _u16p)
+        self.lib.dg_ref_k_grouped_tn(_p(A, _u8p), _p(sa, _f32p), sa.shape[-1], _p(B, _u8p),
+                                     _p(sb, _f32p), cp, _p(D, _u16p), M, N, _p(ks, _i32p), G,
+                                     nthreads)
         return D
 
     def gemm_nt_rows(self, A, sa, B, sb, rows, nthreads=0):

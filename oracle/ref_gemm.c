@@ -28,7 +28,9 @@
  * round in double (relative error ~1e-16).  The result is rounded once, from
  * double straight to bf16, round-to-nearest-even.
  *
- * The file also holds the activation quantiser that produces A and sa
+ * The file also holds the other storage layouts (nn, tn, tt) and the
+ * K-grouped form (dg_ref_gemm_layout, dg_ref_k_grouped_tn, with their
+ * readings) and the activation quantiser that produces A and sa
  * (dg_ref_quantize_1x128, at the end, with its own reading).
  *
  * The M-grouped forms (same pages, section "Dense y Grouped GEMM"):
@@ -342,6 +344,104 @@ void dg_ref_grouped_masked(const uint8_t *A, const float *sa, int ld_sa,
             free(acc);
         }
     }
+}
+
+/* ------------------------------------------- operand layouts ----------- */
+/* The four storage layouts of the non-grouped GEMM, named after DeepGEMM's
+ * fp8_gemm_{nt, nn, tn, tt} (es.news.hada.io/topic?id=19459, "Dense y Grouped
+ * GEMM"; all four exist on SM100, "Interfaz GEMM y restricciones de layout").
+ * The naming convention is D = C + A @ B with the letters saying whether each
+ * stored operand enters transposed: "nt" is D = C + A @ B.T.  So
+ *   A "n": stored [M][K], element (m, k) at A[m*K + k]
+ *   A "t": stored [K][M], element (m, k) at A[k*M + m]
+ *   B "t": stored [N][K], element (n, k) at B[n*K + k]
+ *   B "n": stored [K][N], element (n, k) at B[k*N + n]
+ * The scales do not depend on the storage: sa[g*ld_sa + m] per (row, K group),
+ * sb[(n/128)*kb + g] per 128x128 block of (n, k). */
+static double ref_elem(const uint8_t *A, int a_t, const float *sa, int ld_sa,
+                       const uint8_t *B, int b_n, const float *sb, int kb_all,
+                       int M, int N, int K, int m, int n, int g0, int g1)
+{
+    double total = 0.0;
+    for (int g = g0; g < g1; ++g) {
+        double dot = 0.0;
+        for (int k = 128 * g; k < 128 * g + 128; ++k) {
+#if DG_REF_MUTANT == 15
+            uint8_t a = A[(size_t)m * K + k];        /* mutant: A's storage ignored */
+            (void)a_t;
+#else
+            uint8_t a = a_t ? A[(size_t)k * M + m] : A[(size_t)m * K + k];
+#endif
+            uint8_t b = b_n ? B[(size_t)k * N + n] : B[(size_t)n * K + k];
+            dot += dg_ref_e4m3_to_double(a) * dg_ref_e4m3_to_double(b);
+        }
+        total += dot * (double)sa[(size_t)g * ld_sa + m] * (double)sb[(size_t)(n / 128) * kb_all + g];
+    }
+    return total;
+}
+
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* D [M][N] = bf16(C + A @ B) in the layout (a_t, b_n) above; C [M][N] bf16 or
+ * NULL (no addend). */
+void dg_ref_gemm_layout(const uint8_t *A, int a_t, const float *sa, int ld_sa,
+                        const uint8_t *B, int b_n, const float *sb,
+                        const uint16_t *C, uint16_t *D, int M, int N, int K, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = ref_elem(A, a_t, sa, ld_sa, B, b_n, sb, K / 128, M, N, K, m, n, 0, K / 128);
+            double c = C ? bf16_bits_to_double(C[(size_t)m * N + n]) : 0.0;
+            D[(size_t)m * N + n] = dg_ref_bf16_rne(c + acc);
+        }
+}
+
+/* ----------------------------------------------- K-grouped ("tn") -------- */
+/* The K-grouped GEMM for the MoE weight gradient (k_grouped_fp8_gemm_tn_contiguous,
+ * same page, "Dense y Grouped GEMM": M and N fixed, the groups concatenated
+ * along K).  Group g owns K rows [k0_g, k0_g + ks[g]) with k0_g = ks[0] + ... +
+ * ks[g-1], each ks[g] a multiple of 128 (whole K groups):
+ *   D[g][m][n] = bf16( C[g][m][n] + sum over the K groups j of group g of
+ *                      (sum_{k in j} dec(A[k][m]) dec(B[k][n])) sa[j][m] sb[n/128][j] )
+ * A: [K_all][M] ("t"), B: [K_all][N] ("n"), sa: [K_all/128][ld_sa],
+ * sb: [ceil(N/128)][K_all/128], C and D: [G][M][N] (C may be NULL).  A group
+ * with ks[g] = 0 gives D = C (or +0). */
+void dg_ref_k_grouped_tn(const uint8_t *A, const float *sa, int ld_sa,
+                         const uint8_t *B, const float *sb, const uint16_t *C,
+                         uint16_t *D, int M, int N, const int32_t *ks, int num_groups,
+                         int nthreads)
+{
+    int K_all = 0;
+    for (int g = 0; g < num_groups; ++g)
+        K_all += ks[g];
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int g = 0; g < num_groups; ++g)
+        for (int m = 0; m < M; ++m) {
+            int k0 = 0;
+            for (int h = 0; h < g; ++h)
+                k0 += ks[h];
+#if DG_REF_MUTANT == 14
+            if (g > 0 && k0 >= 128)
+                k0 -= 128;                /* mutant: segment starts a K group early */
+#endif
+            int g0 = k0 / 128, g1 = (k0 + ks[g]) / 128;
+            for (int n = 0; n < N; ++n) {
+                double acc = ref_elem(A, 1, sa, ld_sa, B, 1, sb, K_all / 128, M, N, K_all, m, n,
+                                      g0, g1);
+                size_t o = ((size_t)g * M + m) * N + n;
+                double c = C ? bf16_bits_to_double(C[o]) : 0.0;
+                D[o] = dg_ref_bf16_rne(c + acc);
+            }
+        }
 }
 
 /* ------------------------------------------------ activation quantiser -- */

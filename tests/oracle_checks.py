@@ -393,6 +393,63 @@ def check_gemm_with_c(orc, seed=37):
     assert np.array_equal(orc.gemm_nt_c(A, sa, B, sb, Cb), want)
 
 
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def check_gemm_layouts(orc, seed=41):
+    """nn / tn / tt against gemm_nt on the same logical operands, transposed
+    here by numpy (M, N, K all different and N ragged, so a swapped or
+    transposed index cannot pass); "nt" through the layout routine equals
+    gemm_nt; the addend enters as in gemm_nt_c."""
+    p = W.dense_problem(40, 136, 384, seed)
+    A, B, sa, sb = p["A"], p["B"], p["sa"], p["sb"]
+    At, Bt = np.ascontiguousarray(A.T), np.ascontiguousarray(B.T)   # [K, M], [K, N]
+    want = orc.gemm_nt(A, sa, B, sb)
+    stored = {"nt": (A, B), "nn": (A, Bt), "tn": (At, Bt), "tt": (At, B)}
+    for layout, (a, b) in stored.items():
+        got = orc.gemm_layout(layout, a, sa, b, sb)
+        assert np.array_equal(got, want), f"layout {layout}"
+    rng = np.random.default_rng(seed)
+    C = _bf16_bits(rng.standard_normal((40, 136)))
+    assert np.array_equal(orc.gemm_layout("tn", At, sa, Bt, sb, C), orc.gemm_nt_c(A, sa, B, sb, C))
+
+
+def check_k_grouped(orc, seed=43):
+    """K-grouped tn: each group equals gemm_nt_c on its own K slice (operands
+    transposed by numpy, the slice's scale rows and columns), an empty group
+    returns C (or +0) bit for bit, and one group over all of K equals the tn
+    layout."""
+    rng = np.random.default_rng(seed)
+    M, N = 40, 136
+    ks = np.array([256, 0, 384, 128], np.int32)
+    K_all = int(ks.sum())
+    kb = K_all // 128
+    A = W.random_codes((K_all, M), seed + 1)             # [K_all, M]
+    B = W.random_codes((K_all, N), seed + 2)             # [K_all, N]
+    sa = (rng.random((kb, W.tma_aligned_ld(M))) + 0.25).astype(np.float32)
+    sb = (rng.random(((N + 127) // 128, kb)) + 0.25).astype(np.float32)
+    C = _bf16_bits(rng.standard_normal((len(ks), M, N)))
+    D = orc.k_grouped_tn(A, sa, B, sb, ks, C)
+    D0 = orc.k_grouped_tn(A, sa, B, sb, ks)
+    k0 = 0
+    for g, kg in enumerate(ks):
+        if kg == 0:
+            assert np.array_equal(D[g], C[g]), f"empty group {g} must return C"
+            assert not np.any(D0[g]), f"empty group {g} without C must be +0"
+            continue
+        j0, j1 = k0 // 128, (k0 + kg) // 128
+        Ag = np.ascontiguousarray(A[k0:k0 + kg].T)
+        Bg = np.ascontiguousarray(B[k0:k0 + kg].T)
+        sag = np.ascontiguousarray(sa[j0:j1])
+        sbg = np.ascontiguousarray(sb[:, j0:j1])
+        assert np.array_equal(D[g], orc.gemm_nt_c(Ag, sag, Bg, sbg, C[g])), f"group {g}"
+        assert np.array_equal(D0[g], orc.gemm_nt(Ag, sag, Bg, sbg)), f"group {g} without C"
+        k0 += kg
+    one = orc.k_grouped_tn(A, sa, B, sb, np.array([K_all], np.int32))
+    assert np.array_equal(one[0], orc.gemm_layout("tn", A, sa, B, sb))
+
+
 # ------------------------------------------------- activation quantiser --
 def _torch_e4m3_bits(v):
     """torch's float32 -> float8_e4m3fn cast of v clamped to +-448 (its cast
@@ -457,6 +514,7 @@ def check_quantize_invariants(orc, seed=31):
 
 
 ALL_CHECKS = [
+    check_gemm_layouts, check_k_grouped,
     check_e4m3_golden, check_e4m3_all_codes, check_bf16_golden, check_bf16_bruteforce,
     check_bf16_vs_torch_float32, check_gemm_bruteforce, check_gemm_exact_integers,
     check_gemm_identity, check_gemm_linearity_transpose, check_gemm_closed_form,

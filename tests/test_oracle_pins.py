@@ -5,7 +5,8 @@ compiles the oracle again with one planted mistake at a time (a dropped K
 group, a transposed scale index, a flushed subnormal, truncation instead of
 round-to-nearest-even, a dropped sign, a transposed operand, a dropped scale,
 padding rows computed, the mask ignored, the quantiser's 448 left out,
-truncation in the e4m3 encoder, the addend C dropped) and shows that at least one check
+truncation in the e4m3 encoder, the addend C dropped, a K-grouped segment
+starting one K group early, A's storage layout ignored) and shows that at least one check
 fails for each, so the checks are able to see such mistakes.
 """
 import pytest
@@ -39,6 +40,8 @@ MUTANTS = {
     11: "quantiser scale without 448",
     12: "e4m3 encode truncates",
     13: "addend C dropped",
+    14: "k-grouped segment starts a K group early",
+    15: "A's storage layout ignored",
 }
 
 
