@@ -57,7 +57,8 @@ typedef enum dg_status {
   DG_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed */
   DG_ERR_TIMEOUT = 7,           /* device: an internal wait gave up */
   DG_ERR_MASK_RANGE = 8,        /* device: masked_m[g] outside [0, max_m] (clamped) */
-  DG_ERR_EXPERT_RANGE = 9       /* device: m_indices outside [-1, G) or a 128-row block mixes experts */
+  DG_ERR_EXPERT_RANGE = 9,      /* device: m_indices outside [-1, G) or a 128-row block mixes experts */
+  DG_ERR_KS_RANGE = 10          /* device: ks[g] negative, not a multiple of 128, or past K_total */
 } dg_status;
 
 /* Dense GEMM (DeepGEMM "gemm_fp8_fp8_bf16_nt", deepep.org/zh/deepgemm, "接口设计").
@@ -77,6 +78,53 @@ dg_status dg_gemm_fp8_fp8_bf16_nt(const void* A, const float* sa, int ld_sa, con
 dg_status dg_gemm_fp8_fp8_bf16_nt_add_c(const void* A, const float* sa, int ld_sa, const void* B,
                                         const float* sb, const void* C, void* D, int M, int N,
                                         int K, void* stream);
+
+/* The dense GEMM in the other storage layouts (DeepGEMM's fp8_gemm_{nn, tn, tt},
+ * es.news.hada.io/topic?id=19459, "Dense y Grouped GEMM"; all four layouts
+ * on SM100, "Interfaz GEMM y restricciones de layout").  The letters say
+ * whether each stored operand enters D = C + A @ B transposed:
+ *   nn  A [M][K], B [K][N]      tn  A [K][M], B [K][N]      tt  A [K][M], B [N][K]
+ * (nt, above: A [M][K], B [N][K]).  The scales do not move with the operands:
+ * sa [K/128][ld_sa] one per (row m, K group), sb [ceil(N/128)][K/128] one per
+ * 128 x 128 block of (n, k); D and the optional addend C (null: none; may be
+ * D itself) bf16 [M][N].  Per element the result is
+ *   D[m,n] = bf16( C[m,n] + sum_g (sum_{k in g} A(m,k) B(n,k)) sa[g][m] sb[n/128][g] ).
+ * Requirements as for dg_gemm_fp8_fp8_bf16_nt, and M a multiple of 16 when A
+ * is stored [K][M] (a row of it is M bytes), else DG_ERR_UNSUPPORTED_SHAPE. */
+dg_status dg_gemm_fp8_fp8_bf16_nn(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream);
+dg_status dg_gemm_fp8_fp8_bf16_tn(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream);
+dg_status dg_gemm_fp8_fp8_bf16_tt(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream);
+
+/* K-grouped GEMM for the MoE weight gradient (DeepGEMM
+ * "k_grouped_fp8_gemm_tn_contiguous", es.news.hada.io/topic?id=19459, "Dense
+ * y Grouped GEMM": M and N fixed, the groups concatenated along K).  Group g
+ * owns the K rows [k0_g, k0_g + ks[g]), k0_g = ks[0] + ... + ks[g-1]:
+ *   D[g][m][n] = bf16( C[g][m][n] + sum over the K groups j of group g of
+ *                      (sum_{k in j} A[k][m] B[k][n]) sa[j][m] sb[n/128][j] )
+ *   A   e4m3 [K_total][M] ("t"), B e4m3 [K_total][N] ("n")
+ *   sa  fp32 [K_total/128][ld_sa], sb fp32 [ceil(N/128)][K_total/128]
+ *   C   bf16 [num_groups][M][N] or null (none); it may be D itself
+ *   D   bf16 [num_groups][M][N]
+ *   ks  int32 [num_groups] on the device (read by the kernel, never by the
+ *       host, so a captured graph follows new values): each a multiple of 128,
+ *       >= 0, summing to at most K_total.  A group with ks[g] = 0 gets D = C
+ *       (or +0).  A bad entry is clamped (to whole K groups within K_total)
+ *       and reported as DG_ERR_KS_RANGE by dg_get_device_status.
+ * Requirements (host-checked): 1 <= num_groups <= 1024; K_total a positive
+ * multiple of 128 up to 65536; M and N multiples of 16; ld_sa >= M, a
+ * multiple of 4; A, B, C, D, sa 16-byte aligned, sb and ks 4-byte aligned.
+ * M == 0 is a no-op. */
+dg_status dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(const void* A, const float* sa, int ld_sa,
+                                                       const void* B, const float* sb,
+                                                       const void* C, void* D, const int32_t* ks,
+                                                       int num_groups, int M, int N, int K_total,
+                                                       void* stream);
 
 /* M-grouped GEMM, contiguous layout (DeepGEMM "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous";
  * es.news.hada.io/topic?id=19459, "Dense y Grouped GEMM": the experts' rows are
@@ -155,12 +203,14 @@ const char* dg_last_error_string(void);
 
 /* Waits for `stream`, then returns and clears the device status word of the
  * current device: DG_OK, or the first device-side error recorded since the last
- * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE). */
+ * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE, DG_ERR_KS_RANGE). */
 dg_status dg_get_device_status(void* stream);
 
 /* Tile configuration the library would choose (heuristic; no device needed).
- * kind: 0 dense, 1 contiguous, 2 masked.  m is M (dense), M_total
- * (contiguous) or expected_m (masked).  num_sms is the SM count to plan for.
+ * kind: 0 dense (nt), 1 contiguous, 2 masked, 3 K-grouped (tn).  m is M
+ * (dense, K-grouped), M_total (contiguous) or expected_m (masked); k is K
+ * (K-grouped: K_total, planned as num_groups equal groups).  num_sms is the
+ * SM count to plan for.
  * With a GB300 as the current device (and num_sms at most its SM count), the
  * clusters that fit at once are the device's, so the result is the
  * configuration a launch on num_sms SMs takes; without one, num_sms / S

@@ -14,6 +14,8 @@ import os
 
 __all__ = [
     "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "gemm_fp8_fp8_bf16_nt_add_c",
+    "gemm_fp8_fp8_bf16_nn", "gemm_fp8_fp8_bf16_tn", "gemm_fp8_fp8_bf16_tt",
+    "k_grouped_gemm_fp8_fp8_bf16_tn_contiguous",
     "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
@@ -27,12 +29,14 @@ LIB_PATH = os.path.join(HERE, "libdg.so")
 STATUS_NAMES = {
     0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED_SHAPE", 3: "DG_ERR_MISALIGNED",
     4: "DG_ERR_NO_DEVICE", 5: "DG_ERR_ARCH", 6: "DG_ERR_CUDA", 7: "DG_ERR_TIMEOUT",
-    8: "DG_ERR_MASK_RANGE", 9: "DG_ERR_EXPERT_RANGE",
+    8: "DG_ERR_MASK_RANGE", 9: "DG_ERR_EXPERT_RANGE", 10: "DG_ERR_KS_RANGE",
 }
 
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = [
     "dg_gemm_fp8_fp8_bf16_nt", "dg_gemm_fp8_fp8_bf16_nt_add_c",
+    "dg_gemm_fp8_fp8_bf16_nn", "dg_gemm_fp8_fp8_bf16_tn", "dg_gemm_fp8_fp8_bf16_tt",
+    "dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
     "dg_set_num_sms",
@@ -72,6 +76,11 @@ def lib():
         L.dg_gemm_fp8_fp8_bf16_nt.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]
         L.dg_gemm_fp8_fp8_bf16_nt_add_c.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                                     _vp]
+        for name in ("nn", "tn", "tt"):
+            getattr(L, "dg_gemm_fp8_fp8_bf16_" + name).argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp,
+                                                                   _i, _i, _i, _vp]
+        L.dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked.argtypes = [
@@ -135,6 +144,33 @@ def gemm_fp8_fp8_bf16_nt_add_c(A, sa, ld_sa, B, sb, C, D, M, N, K, stream=None):
     """D[M,N] = bf16(C + sum_g (A_g B_g^T) sa sb); C may be D."""
     _check(lib().dg_gemm_fp8_fp8_bf16_nt_add_c(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb),
                                                _ptr(C), _ptr(D), M, N, K, _stream(stream)))
+
+
+def gemm_fp8_fp8_bf16_nn(A, sa, ld_sa, B, sb, D, M, N, K, C=None, stream=None):
+    """D[M,N] = bf16(C + A @ B): A [M,K], B [K,N]; C optional (may be D)."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_nn(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(C),
+                                         _ptr(D), M, N, K, _stream(stream)))
+
+
+def gemm_fp8_fp8_bf16_tn(A, sa, ld_sa, B, sb, D, M, N, K, C=None, stream=None):
+    """D[M,N] = bf16(C + A^T @ B): A [K,M], B [K,N]; C optional (may be D)."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_tn(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(C),
+                                         _ptr(D), M, N, K, _stream(stream)))
+
+
+def gemm_fp8_fp8_bf16_tt(A, sa, ld_sa, B, sb, D, M, N, K, C=None, stream=None):
+    """D[M,N] = bf16(C + A^T @ B^T): A [K,M], B [N,K]; C optional (may be D)."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_tt(_ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(C),
+                                         _ptr(D), M, N, K, _stream(stream)))
+
+
+def k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(A, sa, ld_sa, B, sb, D, ks, num_groups, M, N,
+                                              K_total, C=None, stream=None):
+    """D[g] = bf16(C[g] + A_g^T B_g) over each group's K rows: A [K_total,M],
+    B [K_total,N], ks int32 [G] on the device, D (and C) [G,M,N]."""
+    _check(lib().dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(
+        _ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(C), _ptr(D), _ptr(ks), num_groups, M, N,
+        K_total, _stream(stream)))
 
 
 def m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(A, sa, ld_sa, B, sb, D, m_indices, M_total, N, K,

@@ -81,16 +81,28 @@ struct Table {
   int n;
 };
 
-Table table_for(int kind) {
+// Instance tables: 0 dense nt, 1 contiguous, 2 masked, 3 MN-major operands
+// (dense nn / tn / tt and the K-grouped form).
+constexpr int kNumTables = 4;
+
+int table_id(int kind, int layout) {
+  return (layout != dgk::kNT || kind == dgk::kKGrouped) ? 3 : kind;
+}
+
+Table table_for(int tid) {
   Table t{nullptr, 0};
-  if (kind == dgk::kDense) t.p = dgk::instances_dense(&t.n);
-  else if (kind == dgk::kContiguous) t.p = dgk::instances_contiguous(&t.n);
-  else t.p = dgk::instances_masked(&t.n);
+  if (tid == 0) t.p = dgk::instances_dense(&t.n);
+  else if (tid == 1) t.p = dgk::instances_contiguous(&t.n);
+  else if (tid == 2) t.p = dgk::instances_masked(&t.n);
+  else t.p = dgk::instances_mn(&t.n);
   return t;
 }
 
 int smem_for(const Instance& in, int kb, int num_groups) {
-  int s = in.fixed_smem + 3 * kb * 4 + (in.mode == dgk::kMasked ? (2 * num_groups + 1) * 4 : 0);
+  int s = in.fixed_smem + 3 * kb * 4 +
+          (in.mode == dgk::kMasked     ? (2 * num_groups + 1) * 4
+           : in.mode == dgk::kKGrouped ? (num_groups + 1) * 4
+                                       : 0);
   return (s + 15) & ~15;
 }
 
@@ -162,15 +174,19 @@ bool has_split64(const Table& tab) {
 }
 
 // cap(S): clusters of S CTAs that can be resident at once.
+// K-grouped form: k is the whole K (the operands' rows); the model takes each
+// tile as an average group's K, k / num_groups.
 template <typename Cap>
 Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sms, Cap cap,
-            int force_bn, int force_split) {
-  const Table tab = table_for(kind);
+            int force_bn, int force_split, int layout = dgk::kNT) {
+  const Table tab = table_for(table_id(kind, layout));
   const int kb = k / 128;
+  const int k_model = kind == dgk::kKGrouped ? std::max(128, (k / std::max(1, num_groups)) / 128 * 128) : k;
   Plan best;
   double best_cost = 1e300;
   for (int i = 0; i < tab.n; ++i) {
     const Instance& in = tab.p[i];
+    if (in.mode != kind || in.layout != layout) continue;
     if (force_bn > 0 && in.block_n != force_bn) continue;
     // 64-row A tiles serve M <= 64 only, and are the choice there
     if (in.a_rows < 128 && m_rows > in.a_rows) continue;
@@ -199,11 +215,12 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
         continue;
       }
       long long mblk;
-      if (kind == dgk::kMasked) mblk = (long long)num_groups * cdiv(m_rows, 128);
+      if (kind == dgk::kMasked || kind == dgk::kKGrouped)
+        mblk = (long long)num_groups * cdiv(m_rows, 128);
       else mblk = cdiv(m_rows, in.pair ? 256 : 128);
       const long long tiles = mblk * cdiv(n, in.block_n);
       const long long c = std::max(1, cap(i, in, in.pair ? 2 : S, smem));
-      const double t = est_time_us(in, S, tiles, c, num_sms, kind, m_rows, n, k, num_groups);
+      const double t = est_time_us(in, S, tiles, c, num_sms, kind, m_rows, n, k_model, num_groups);
       const double cost = t;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
@@ -230,8 +247,8 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   unsigned int* status = nullptr;
-  // resident clusters per (form, instance, split)
-  int max_clusters[3][8][kMaxCluster + 1] = {};
+  // resident clusters per (instance table, instance, split)
+  int max_clusters[kNumTables][16][kMaxCluster + 1] = {};
 };
 
 std::mutex g_mu;
@@ -280,8 +297,8 @@ dg_status device_state(DeviceState** out, int* dev_out) {
       return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled not available");
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  for (int kind = 0; kind < 3; ++kind) {
-    const Table tab = table_for(kind);
+  for (int tid = 0; tid < kNumTables; ++tid) {
+    const Table tab = table_for(tid);
     for (int i = 0; i < tab.n; ++i)
       if ((e = tab.p[i].set_smem(kMaxSmem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
@@ -296,7 +313,7 @@ dg_status device_state(DeviceState** out, int* dev_out) {
 int clusters_resident(DeviceState& st, int kind, int inst, const Instance& in, int S, int smem,
                       int num_sms) {
   if (S <= 1) return num_sms;
-  int& slot = st.max_clusters[kind][inst][S];
+  int& slot = st.max_clusters[table_id(kind, in.layout)][inst][S];
   if (slot == 0) {
     int n = 0;
     if (in.max_clusters(S, kMaxSmem, &n) != cudaSuccess || n <= 0) {
@@ -330,23 +347,30 @@ dg_status encode(CUtensorMap* m, CUtensorMapDataType dt, void* ptr, const uint64
   return DG_OK;
 }
 
-// A [z][rows][K] e4m3, B [g][N][K] e4m3, sa [z][kb][ld_sa] fp32, D [z][rows][N] bf16.
+// A [z][rows][K] e4m3 (layout bit 0: [K][rows]), B [g][N][K] e4m3 (layout
+// bit 1: [K][N]), sa [z][kb][ld_sa] fp32, D and C [zD][rows][N] bf16 (zD = zA
+// unless given).  MN-major operands are read in boxes of 128 x 128 K rows.
 dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, const void* B,
                     void* D, int rows, int zA, int N, int K, int gB, int block_n, int a_rows,
-                    const void* C = nullptr) {
+                    const void* C = nullptr, int layout = dgk::kNT, int zD = 0) {
   const int kb = K / 128;
+  if (zD <= 0) zD = zA;
   {
-    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)zA};
-    const uint64_t str[2] = {(uint64_t)K, (uint64_t)rows * K};
-    const uint32_t box[3] = {128, (uint32_t)a_rows, 1};
+    const bool mn = (layout & 1) != 0;
+    const uint64_t dims[3] = {mn ? (uint64_t)rows : (uint64_t)K, mn ? (uint64_t)K : (uint64_t)rows,
+                              (uint64_t)zA};
+    const uint64_t str[2] = {mn ? (uint64_t)rows : (uint64_t)K, (uint64_t)rows * K};
+    const uint32_t box[3] = {128, mn ? 128u : (uint32_t)a_rows, 1};
     dg_status s = encode(&mp->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(A), dims, str,
                          box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A");
     if (s != DG_OK) return s;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)gB};
-    const uint64_t str[2] = {(uint64_t)K, (uint64_t)N * K};
-    const uint32_t box[3] = {128, (uint32_t)block_n, 1};
+    const bool mn = (layout & 2) != 0;
+    const uint64_t dims[3] = {mn ? (uint64_t)N : (uint64_t)K, mn ? (uint64_t)K : (uint64_t)N,
+                              (uint64_t)gB};
+    const uint64_t str[2] = {mn ? (uint64_t)N : (uint64_t)K, (uint64_t)N * K};
+    const uint32_t box[3] = {128, mn ? 128u : (uint32_t)block_n, 1};
     dg_status s = encode(&mp->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(B), dims, str,
                          box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
     if (s != DG_OK) return s;
@@ -361,7 +385,7 @@ dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, co
     if (s != DG_OK) return s;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)rows, (uint64_t)zA};
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)rows, (uint64_t)zD};
     const uint64_t str[2] = {(uint64_t)N * 2, (uint64_t)rows * N * 2};
     const uint32_t box[3] = {32, 128, 1};
     dg_status s = encode(&mp->d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, dims, str, box,
@@ -386,21 +410,33 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 namespace {
 
 const char* kind_name(int kind) {
-  return kind == dgk::kDense ? "dense" : kind == dgk::kContiguous ? "contiguous" : "masked";
+  return kind == dgk::kDense        ? "dense"
+         : kind == dgk::kContiguous ? "contiguous"
+         : kind == dgk::kMasked     ? "masked"
+                                    : "k-grouped";
 }
 
-// Shared path of the three GEMM entry points.  rows = M (dense), M_total
-// (contiguous) or max_m (masked); idx = m_indices or masked_m.
+const char* layout_name(int layout) {
+  return layout == dgk::kNT ? "nt" : layout == dgk::kNN ? "nn" : layout == dgk::kTN ? "tn" : "tt";
+}
+
+// Shared path of the GEMM entry points.  rows = M (dense, K-grouped), M_total
+// (contiguous) or max_m (masked); idx = m_indices, masked_m or ks; K = the
+// whole K (K-grouped: the operands' rows, all groups together).
 dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B, const float* sb,
               void* D, const int32_t* idx, int rows, int N, int K, int G, int expected_m,
-              void* stream, const void* C = nullptr) {
+              void* stream, const void* C = nullptr, int layout = dgk::kNT) {
   read_env_once();
   // -------- validation (host only; nothing is launched on an error) ------
   if (rows < 0 || N < 0 || K < 0)
     return fail(DG_ERR_INVALID_ARG, "negative size (rows=%d, N=%d, K=%d)", rows, N, K);
-  if (kind != dgk::kDense && (G < 1 || (kind == dgk::kMasked && G > dgk::MAX_GROUPS_MASKED)))
-    return fail(DG_ERR_INVALID_ARG, "num_groups=%d outside [1, %d]", G,
-                kind == dgk::kMasked ? dgk::MAX_GROUPS_MASKED : 0x7fffffff);
+  const int max_groups = kind == dgk::kMasked     ? dgk::MAX_GROUPS_MASKED
+                         : kind == dgk::kKGrouped ? dgk::MAX_GROUPS_KGROUPED
+                                                  : 0x7fffffff;
+  if (kind != dgk::kDense && (G < 1 || G > max_groups))
+    return fail(DG_ERR_INVALID_ARG, "num_groups=%d outside [1, %d]", G, max_groups);
+  if ((layout & 1) && rows % 16 != 0)
+    return fail(DG_ERR_UNSUPPORTED_SHAPE, "M=%d: A stored [K][M] needs M a multiple of 16", rows);
   if (K % 128 != 0 || K < 128 || K > 128 * dgk::MAX_KB)
     return fail(DG_ERR_UNSUPPORTED_SHAPE, "K=%d: need a multiple of 128 in [128, %d]", K,
                 128 * dgk::MAX_KB);
@@ -411,7 +447,8 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   if (!A || !sa || !B || !sb || !D)
     return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
   if (kind != dgk::kDense && !idx)
-    return fail(DG_ERR_INVALID_ARG, "null %s", kind == dgk::kMasked ? "masked_m" : "m_indices");
+    return fail(DG_ERR_INVALID_ARG, "null %s",
+                kind == dgk::kMasked ? "masked_m" : kind == dgk::kKGrouped ? "ks" : "m_indices");
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sa) || (C && !aligned16(C)) ||
       (reinterpret_cast<uintptr_t>(sb) & 3u) || (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
     return fail(DG_ERR_MISALIGNED, "A, B, C, D and sa need 16-byte alignment, sb and indices 4");
@@ -433,11 +470,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   };
   const int m_plan = kind == dgk::kMasked ? std::max(1, std::min(expected_m, rows)) : rows;
   const Plan pl = choose(kind, m_plan, N, K, G, num_sms, cap, g_force_bn.load(),
-                         g_force_split.load());
+                         g_force_split.load(), layout);
   if (pl.inst < 0)
     return fail(DG_ERR_UNSUPPORTED_SHAPE, "no kernel configuration for this shape%s",
                 g_force_bn.load() > 0 ? " (DG_FORCE_CONFIG)" : "");
-  const Instance& in = table_for(kind).p[pl.inst];
+  const Instance& in = table_for(table_id(kind, layout)).p[pl.inst];
   int clusters = pl.clusters;
   if (kind == dgk::kMasked) {
     const long long ub = (long long)G * cdiv(rows, 128) * cdiv(N, in.block_n);
@@ -446,9 +483,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   const int grid = std::max(1, clusters) * (in.pair ? 2 : pl.split);
 
   dgk::Maps maps;
+  const bool has_c = kind == dgk::kDense || kind == dgk::kKGrouped;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
-                kind == dgk::kDense ? 1 : G, in.pair ? in.block_n / 2 : in.block_n, in.a_rows,
-                kind == dgk::kDense ? C : nullptr);
+                (kind == dgk::kDense || kind == dgk::kKGrouped) ? 1 : G,
+                in.pair ? in.block_n / 2 : in.block_n, in.a_rows, has_c ? C : nullptr, layout,
+                kind == dgk::kKGrouped ? G : 0);
   if (s != DG_OK) return s;
 
   dgk::Params p{};
@@ -458,6 +497,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.kb = K / 128;
   p.nb = (N + 127) / 128;
   p.num_groups = kind == dgk::kDense ? 1 : G;
+  p.ks = kind == dgk::kKGrouped ? idx : nullptr;
   p.num_m_blocks = (int)cdiv(rows, in.pair ? 256 : 128);
   p.num_n_blocks = (int)cdiv(N, in.block_n);
   p.raster_m = kRasterM;
@@ -466,7 +506,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
   p.masked_m = kind == dgk::kMasked ? idx : nullptr;
   p.D = static_cast<uint16_t*>(D);
-  p.C = static_cast<const uint16_t*>(C);
+  p.C = has_c ? static_cast<const uint16_t*>(C) : nullptr;
   p.status = st->status;
   p.timeout_ns = g_timeout_ns.load();
   p.debug_flags = g_skip_producer.load() ? dgk::DBG_SKIP_PRODUCER : 0u;
@@ -479,9 +519,9 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   }
   if (print_configs())
     std::fprintf(stderr,
-                 "[dg] %s M=%d N=%d K=%d G=%d: block_n=%d split_k=%d stages=%d tiles=%lld "
+                 "[dg] %s %s M=%d N=%d K=%d G=%d: block_n=%d split_k=%d stages=%d tiles=%lld "
                  "grid=%d smem=%d\n",
-                 kind_name(kind), rows, N, K, G, in.block_n, pl.split, in.stages,
+                 kind_name(kind), layout_name(layout), rows, N, K, G, in.block_n, pl.split, in.stages,
                  (long long)pl.tiles, grid, pl.smem);
   return ok();
 }
@@ -501,6 +541,33 @@ dg_status dg_gemm_fp8_fp8_bf16_nt_add_c(const void* A, const float* sa, int ld_s
                                         int K, void* stream) {
   if (!C) return fail(DG_ERR_INVALID_ARG, "null addend C (use dg_gemm_fp8_fp8_bf16_nt)");
   return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream, C);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_nn(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream) {
+  return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream, C, dgk::kNN);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_tn(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream) {
+  return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream, C, dgk::kTN);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_tt(const void* A, const float* sa, int ld_sa, const void* B,
+                                  const float* sb, const void* C, void* D, int M, int N, int K,
+                                  void* stream) {
+  return run(dgk::kDense, A, sa, ld_sa, B, sb, D, nullptr, M, N, K, 1, M, stream, C, dgk::kTT);
+}
+
+dg_status dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(const void* A, const float* sa, int ld_sa,
+                                                       const void* B, const float* sb,
+                                                       const void* C, void* D, const int32_t* ks,
+                                                       int num_groups, int M, int N, int K_total,
+                                                       void* stream) {
+  return run(dgk::kKGrouped, A, sa, ld_sa, B, sb, D, ks, M, N, K_total, num_groups, M, stream, C,
+             dgk::kTN);
 }
 
 dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(const void* A, const float* sa, int ld_sa,
@@ -606,6 +673,8 @@ dg_status dg_get_device_status(void* stream) {
     case dgk::ST_MASK_RANGE: return fail(DG_ERR_MASK_RANGE, "masked_m outside [0, max_m]");
     case dgk::ST_EXPERT_RANGE:
       return fail(DG_ERR_EXPERT_RANGE, "m_indices out of range or a block mixes experts");
+    case dgk::ST_KS_RANGE:
+      return fail(DG_ERR_KS_RANGE, "ks: a negative or partial K group, or past K_total");
     default: return fail(DG_ERR_CUDA, "unknown device status %u", v);
   }
 }
@@ -613,7 +682,7 @@ dg_status dg_get_device_status(void* stream) {
 dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
                          dg_config* out) {
   read_env_once();
-  if (!out || kind < 0 || kind > 2 || m < 1 || n < 16 || n % 16 || k < 128 || k % 128 ||
+  if (!out || kind < 0 || kind > 3 || m < 1 || n < 16 || n % 16 || k < 128 || k % 128 ||
       k > 128 * dgk::MAX_KB || num_sms < 1 || (kind != dgk::kDense && num_groups < 1))
     return fail(DG_ERR_INVALID_ARG, "dg_plan_config: bad arguments");
   const int G = kind == dgk::kDense ? 1 : num_groups;
@@ -635,9 +704,11 @@ dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_
     if (S <= 1) return num_sms;
     return st ? clusters_resident(*st, kind, i, in, S, smem, num_sms) : num_sms / S;
   };
-  const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load());
+  const int layout = kind == dgk::kKGrouped ? dgk::kTN : dgk::kNT;
+  const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load(),
+                         layout);
   if (pl.inst < 0) return fail(DG_ERR_UNSUPPORTED_SHAPE, "no configuration");
-  const Instance& in = table_for(kind).p[pl.inst];
+  const Instance& in = table_for(table_id(kind, layout)).p[pl.inst];
   out->block_m = in.pair ? 2 * dgk::BLOCK_M : dgk::BLOCK_M;
   out->pair = in.pair;
   out->block_n = in.block_n;

@@ -1,0 +1,21 @@
+// Instances with MN-major operands: the dense nn / tn / tt layouts and the
+// K-grouped tn form (A stored [K][M], B stored [K][N]).
+#define DGK_DEFINE_INSTANCES
+#include "dg_instances.cuh"
+
+namespace dgk {
+const Instance* instances_mn(int* count) {
+  static const Instance table[] = {
+      InstanceOf<128, 5, false, kDense, 128, false, kNN>::make(),
+      InstanceOf<256, 3, false, kDense, 128, false, kNN>::make(),
+      InstanceOf<128, 5, false, kDense, 128, false, kTN>::make(),
+      InstanceOf<256, 3, false, kDense, 128, false, kTN>::make(),
+      InstanceOf<128, 5, false, kDense, 128, false, kTT>::make(),
+      InstanceOf<256, 3, false, kDense, 128, false, kTT>::make(),
+      InstanceOf<128, 5, false, kKGrouped, 128, false, kTN>::make(),
+      InstanceOf<256, 3, false, kKGrouped, 128, false, kTN>::make(),
+  };
+  *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
+  return table;
+}
+}  // namespace dgk

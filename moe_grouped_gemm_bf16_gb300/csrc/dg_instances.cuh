@@ -20,6 +20,7 @@ struct Instance {
   int mode;
   int a_rows;      // rows of A per tile loaded by TMA (128, or 64 for M <= 64)
   int pair;        // 1: CTA-pair form (cta_group::2, 256-row tiles over a 2-CTA cluster)
+  int layout;      // operand storage (kNT, kNN, kTN, kTT)
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
                         cudaStream_t s);
@@ -31,6 +32,8 @@ struct Instance {
 const Instance* instances_dense(int* count);
 const Instance* instances_contiguous(int* count);
 const Instance* instances_masked(int* count);
+// dense nn / tn / tt and the K-grouped tn form (MN-major operands)
+const Instance* instances_mn(int* count);
 
 }  // namespace dgk
 
@@ -39,9 +42,10 @@ const Instance* instances_masked(int* count);
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false,
+          int LAYOUT = kNT>
 struct InstanceOf {
-  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS, PAIR>;
+  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS, PAIR, LAYOUT>;
 
   static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
                             cudaStream_t s) {
@@ -89,7 +93,7 @@ struct InstanceOf {
   }
 
   static Instance make() {
-    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0,
+    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0, LAYOUT,
                     SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF + 1024, &launch,
                     &set_smem, &max_clusters};
   }

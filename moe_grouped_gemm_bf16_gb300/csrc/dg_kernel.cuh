@@ -78,16 +78,20 @@ template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false
 __host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
   return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF +
          3 * kb * 4 +
-         (mode == kMasked ? (2 * num_groups + 1) * 4 : 0);
+         (mode == kMasked ? (2 * num_groups + 1) * 4 : mode == kKGrouped ? (num_groups + 1) * 4 : 0);
 }
 
 struct Tile {
   int m0;     // first row of the tile, within its group
   int n0;     // first column
-  int z;      // group coordinate of A / sa / D (masked form), else 0
+  int z;      // group coordinate of A / sa (masked form), else 0
+  int zd;     // group coordinate of D / C (masked and K-grouped forms), else 0
   int e;      // expert / group of B and sb
   int rows;   // rows that hold valid output
-  int skip;   // 1: contiguous padding block (no MMA, +0 output); 2: bad expert id
+  int skip;   // 1: contiguous padding block (no MMA, +0 output); 2: bad expert id;
+              // 3: K-grouped group without K rows (no MMA, D = C or +0)
+  int kbeg;   // the tile's K groups [kbeg, kend) (this CTA's slice in the split form)
+  int kend;
 };
 
 __device__ __forceinline__ void raise_status(const Params& p, unsigned int code) {
@@ -101,11 +105,19 @@ __device__ __forceinline__ void raise_status(const Params& p, unsigned int code)
 // overview deepep.org/zh/deepgemm, "统一优化的块调度器").
 // In the pair form an M block is 256 rows, of which CTA `crank` of the pair
 // owns rows [128 * crank, 128 * crank + 128).
+// K-grouped form: the tiles of group g come before those of g + 1 (each group
+// rasterised alone); `prefix` holds the groups' first K groups.
 template <int BN, int MODE, bool PAIR = false>
 __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_blocks,
-                                            const int* prefix, const int* mcnt,
+                                            const int* prefix, const int* mcnt, int kb0, int kb1,
                                             uint32_t crank = 0) {
   const int nN = p.num_n_blocks;
+  int kg = 0;
+  if (MODE == kKGrouped) {
+    const int per_group = num_m_blocks * nN;
+    kg = t / per_group;
+    t -= kg * per_group;
+  }
   const int band_tiles = p.raster_m * nN;
   const int band = t / band_tiles;
   const int r = t - band * band_tiles;
@@ -115,6 +127,19 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
   Tile T;
   T.n0 = (r / bh) * BN;
   T.skip = 0;
+  T.kbeg = kb0;
+  T.kend = kb1;
+  if (MODE == kKGrouped) {
+    T.m0 = mb * BLOCK_M;
+    T.z = 0;
+    T.e = 0;
+    T.rows = max(0, min(BLOCK_M, p.M - T.m0));
+    T.kbeg = prefix[kg];
+    T.kend = prefix[kg + 1];
+    if (T.kend <= T.kbeg) T.skip = 3;
+    T.zd = kg;
+    return T;
+  }
   if (MODE == kDense) {
     T.m0 = PAIR ? mb * 2 * BLOCK_M + static_cast<int>(crank) * BLOCK_M : mb * BLOCK_M;
     T.z = 0;
@@ -145,6 +170,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
     T.m0 = (mb - prefix[lo]) * BLOCK_M;
     T.rows = min(BLOCK_M, mcnt[lo] - T.m0);
   }
+  T.zd = T.z;
   return T;
 }
 
@@ -194,7 +220,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 namespace dgk {
 
-template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false>
+template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false,
+          int LAYOUT = kNT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
@@ -204,11 +231,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
   static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && (BN == 128 || BN == 256)),
                 "the pair form: dense, full A, 128- or 256-wide tiles");
+  static_assert(LAYOUT == kNT || (!SPLIT && !PAIR && AROWS == BLOCK_M && BN % 128 == 0 &&
+                                   (MODE == kDense || MODE == kKGrouped)),
+                "MN-major operands: dense or K-grouped, full A, 128-multiple tiles");
+  static_assert(MODE != kKGrouped || LAYOUT == kTN, "the K-grouped form is tn");
+  constexpr bool A_MN = (LAYOUT & 1) != 0;     // A stored [K][M]
+  constexpr bool B_MN = (LAYOUT & 2) != 0;     // B stored [K][N]
   using L = SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>;
   constexpr int HALF = BN / PROMO_WG;          // columns per promotion warpgroup
   constexpr int NCH = HALF / 32;               // 32-column TMEM chunks per warpgroup
   // the pair MMA spans both CTAs' 128 rows
-  constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BLOCK_M : BLOCK_M, BN);
+  constexpr uint32_t IDESC = idesc_e4m3_f32(PAIR ? 2 * BLOCK_M : BLOCK_M, BN, A_MN, B_MN);
+  // An MN-major operand slot holds 128 K rows of 128-byte lines per 128-wide
+  // atom (16 KB each, stacked along M / N); the MMA's K step of 32 is then 4
+  // swizzle atoms (4096 bytes) further on, against 32 bytes inside the atom
+  // for a K-major slot.
+  constexpr uint32_t MN_ATOM_BYTES = 128 * BLOCK_K;
+  constexpr uint64_t A_KSTEP = A_MN ? (32 * 128) >> 4 : 32 >> 4;
+  constexpr uint64_t B_KSTEP = B_MN ? (32 * 128) >> 4 : 32 >> 4;
 
   extern __shared__ uint8_t smem_raw[];
   // swizzled tiles need 1024-byte aligned shared-memory addresses
@@ -235,7 +275,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const uint32_t krank = SPLIT ? crank : 0;
   const int kbeg = static_cast<int>(static_cast<long long>(krank) * p.kb / S);
   const int kend = static_cast<int>(static_cast<long long>(krank + 1) * p.kb / S);
-  const int kcnt = kend - kbeg;
 
   // ------------------------------------------------------------- set-up --
   if (threadIdx.x == 0) {
@@ -304,6 +343,35 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     if (lane == 0) prefix[0] = 0;
   }
+  if (MODE == kKGrouped && warp == 2) {
+    // first K group of every group: prefix sum of ks[g] / 128, each ks[g]
+    // checked (>= 0, whole K groups) and the running total clamped to K
+    int carry = 0;
+    bool bad = false;
+    for (int base = 0; base < p.num_groups; base += 32) {
+      const int g = base + lane;
+      int c = 0;
+      if (g < p.num_groups) {
+        const int v = __ldg(p.ks + g);
+        if (v < 0 || (v & (BLOCK_K - 1)) != 0) bad = true;
+        c = max(v, 0) / BLOCK_K;
+      }
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (g < p.num_groups) {
+        if (carry + x > p.kb) bad = true;
+        prefix[g + 1] = min(carry + x, p.kb);
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
+      carry = min(carry, p.kb);
+    }
+    if (lane == 0) prefix[0] = 0;
+    if (bad && blockIdx.x == 0) raise_status(p, ST_KS_RANGE);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -316,7 +384,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
   const uint32_t tmem_base = misc[0];
   const int num_m_blocks = (MODE == kMasked) ? prefix[p.num_groups] : p.num_m_blocks;
-  const int num_tiles = num_m_blocks * p.num_n_blocks;
+  const int num_tiles =
+      num_m_blocks * p.num_n_blocks * (MODE == kKGrouped ? p.num_groups : 1);
   // the split form computes exactly one tile per cluster (the host launches one
   // cluster per tile); the operand ring is reused by its epilogue
   const int tile_stride = SPLIT ? num_tiles : num_clusters;
@@ -341,9 +410,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int s = 0, j = 0;
       uint32_t ph = 0, jph = 0;
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
-        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
+        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
         if (T.skip) continue;
-        for (int g = kbeg; g < kend; ++g) {
+        for (int g = T.kbeg; g < T.kend; ++g) {
           if (wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p)) {
             if constexpr (PAIR) {
               // both CTAs' loads complete on the leader's FULL barrier, which
@@ -355,6 +424,27 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                g * BLOCK_K, T.m0, T.z);
               tma_load_3d_pair(map_cluster(sbase + L::B_OFF + s * L::B_BYTES, crank), &tmB, full,
                                g * BLOCK_K, T.n0 + static_cast<int>(crank) * (BN / 2), T.e);
+            } else if constexpr (LAYOUT != kNT) {
+              // MN-major operands: boxes of 128 (M or N) x 128 K rows; an
+              // MN-major B's boxes wholly past N are not loaded (their columns
+              // are never stored).  A K-major B is one full box as in nt.
+              int nbox = 0;
+              for (int bj = 0; bj < BN / 128; ++bj) nbox += (T.n0 + bj * 128 < p.N) ? 1 : 0;
+              const uint32_t b_bytes = B_MN ? nbox * MN_ATOM_BYTES : L::B_BYTES;
+              mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + b_bytes);
+              const uint32_t a_dst = sbase + L::A_OFF + s * L::A_BYTES;
+              const uint32_t b_dst = sbase + L::B_OFF + s * L::B_BYTES;
+              if constexpr (A_MN)
+                tma_load_3d(a_dst, &tmA, bar(L::FULL + s), T.m0, g * BLOCK_K, T.z);
+              else
+                tma_load_3d(a_dst, &tmA, bar(L::FULL + s), g * BLOCK_K, T.m0, T.z);
+              if constexpr (B_MN) {
+                for (int bj = 0; bj < nbox; ++bj)
+                  tma_load_3d(b_dst + bj * MN_ATOM_BYTES, &tmB, bar(L::FULL + s), T.n0 + bj * 128,
+                              g * BLOCK_K, T.e);
+              } else {
+                tma_load_3d(b_dst, &tmB, bar(L::FULL + s), g * BLOCK_K, T.n0, T.e);
+              }
             } else {
               mbar_arrive_expect_tx(bar(L::FULL + s), L::A_BYTES + L::B_BYTES);
               tma_load_3d(sbase + L::A_OFF + s * L::A_BYTES, &tmA, bar(L::FULL + s), g * BLOCK_K,
@@ -367,7 +457,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
           // the scales of this and the next SA_GROUPS-1 K groups (groups past
           // the tensor's end read as zero and are not used)
-          if ((g - kbeg) % SA_GROUPS == 0) {
+          if ((g - T.kbeg) % SA_GROUPS == 0) {
             if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
               mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
               tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
@@ -416,9 +506,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int s = 0, b = 0, turn = 0;
       uint32_t ph = 0, bph = 0;
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
-        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
+        const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
         if (T.skip) continue;
-        for (int g = kbeg; g < kend; ++g) {
+        for (int g = T.kbeg; g < T.kend; ++g) {
           const bool mine = (turn == me);
           if (++turn == NUM_ISSUERS) turn = 0;
           if (!mine) {
@@ -432,19 +522,23 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           tc_fence_after();
           if (ok_t && ok_f) {
             const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
-            const uint64_t ad = smem_desc_sw128_kmajor(sbase + L::A_OFF + s * L::A_BYTES);
-            const uint64_t bd = smem_desc_sw128_kmajor(sbase + L::B_OFF + s * L::B_BYTES);
+            const uint32_t a_src = sbase + L::A_OFF + s * L::A_BYTES;
+            const uint32_t b_src = sbase + L::B_OFF + s * L::B_BYTES;
+            const uint64_t ad = A_MN ? smem_desc_sw128_mnmajor(a_src, MN_ATOM_BYTES)
+                                     : smem_desc_sw128_kmajor(a_src);
+            const uint64_t bd = B_MN ? smem_desc_sw128_mnmajor(b_src, MN_ATOM_BYTES)
+                                     : smem_desc_sw128_kmajor(b_src);
             if constexpr (PAIR) {
 #pragma unroll
               for (int kk = 0; kk < BLOCK_K / 32; ++kk)
-                mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+                mma_f8f6f4_pair(d, ad + A_KSTEP * kk, bd + B_KSTEP * kk, IDESC, kk > 0 ? 1u : 0u);
               // frees the stage and hands the accumulator over in both CTAs
               mma_commit_pair_multicast(bar(L::EMPTY + s), 0x3);
               mma_commit_pair_multicast(bar(L::T_FULL + b), 0x3);
             } else {
 #pragma unroll
               for (int kk = 0; kk < BLOCK_K / 32; ++kk)
-                mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, IDESC, kk > 0 ? 1u : 0u);
+                mma_f8f6f4(d, ad + A_KSTEP * kk, bd + B_KSTEP * kk, IDESC, kk > 0 ? 1u : 0u);
               mma_commit(bar(L::EMPTY + s));
               mma_commit(bar(L::T_FULL + b));
             }
@@ -476,13 +570,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t cph = 0;                   // phase of the addend's barrier
     float acc[HALF];
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
-      const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, crank);
+      const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
       // Dense form with an addend (D = C + A B^T): thread 0 loads this tile's C
       // into the staging tile, in the store's own layout, halfway through the
       // tile's K groups (the previous tile's store has long finished reading
       // the staging tile by then, and C has long landed by the epilogue).
-      const bool load_c = MODE == kDense && !SPLIT && p.C != nullptr && pt == 0;
-      const int g_c = (T.skip || kcnt == 0) ? -1 : kbeg + kcnt / 2;   // K group after which C loads
+      const bool load_c = (MODE == kDense || MODE == kKGrouped) && !SPLIT && p.C != nullptr && pt == 0;
+      const int tk = T.kend - T.kbeg;     // the tile's K groups
+      const int g_c = (T.skip || tk <= 0) ? -1 : T.kbeg + tk / 2;   // K group after which C loads
       auto issue_c = [&]() {
         bulk_wait_group_read0();
         uint32_t bytes = 0;
@@ -492,17 +587,17 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int cc = 0; cc < BN / 32; ++cc)
           if (T.n0 + cc * 32 < p.N)
             tma_load_3d(out_s + cc * (BLOCK_M * 64), &tmC, bar(L::C_FULL), T.n0 + cc * 32, T.m0,
-                        T.z);
+                        T.zd);
       };
       if (load_c && g_c < 0) issue_c();
       // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
       if (!T.skip) {
         const int blk0 = T.n0 >> 7;
-        for (int i = pt; i < 3 * kcnt; i += 32 * NUM_PROMO_WARPS) {
-          const int jb = i / kcnt, gg = i - jb * kcnt;
+        for (int i = pt; i < 3 * tk; i += 32 * NUM_PROMO_WARPS) {
+          const int jb = i / tk, gg = i - jb * tk;
           const int nbk = min(blk0 + jb, p.nb - 1);
-          sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + kbeg + gg);
+          sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + T.kbeg + gg);
         }
       }
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
@@ -510,7 +605,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
       if (!T.skip) {
         const int nmod = T.n0 & 127;
-        for (int g = kbeg; g < kend; ++g) {
+        for (int g = T.kbeg; g < T.kend; ++g) {
           // hand the TMEM accumulator back to the MMA issuer (pair form: on the
           // leader's barrier); every tcgen05.ld of this warp has completed
           auto release_tmem = [&]() {
@@ -521,7 +616,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               else mbar_arrive(bar(L::T_EMPTY + b));
             }
           };
-          const int r = (g - kbeg) % SA_GROUPS;   // place in the scale slot
+          const int r = (g - T.kbeg) % SA_GROUPS;   // place in the scale slot
           wait_bar(bar(L::T_FULL + b), bph, abort_flag, p);
           if (r == 0) wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
           __syncwarp();
@@ -529,7 +624,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // warps whose TMEM lanes hold no loaded row of A have nothing to add
           if (q * 32 < AROWS) {
           const float a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
-          const float* sbg = sb_s + (g - kbeg);
+          const float* sbg = sb_s + (g - T.kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
           // every outstanding load, so fewer, larger batches expose its latency
@@ -552,7 +647,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               const int c = bt * LB + u;
               const int col = h * HALF + c * 32;
               // the 32 columns lie in one 128-column B scale block
-              const float sc = a_s * sbg[((nmod + col) >> 7) * kcnt];
+              const float sc = a_s * sbg[((nmod + col) >> 7) * tk];
 #pragma unroll
               for (int i = 0; i < 32; i += 2)
                 ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], __uint_as_float(v[u][i]),
@@ -562,7 +657,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           } else {
             release_tmem();
           }
-          if (r == SA_GROUPS - 1 || g == kend - 1) {
+          if (r == SA_GROUPS - 1 || g == T.kend - 1) {
             // the slot's last K group of this tile: hand the slot back
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::SA_EMPTY + j));
@@ -590,7 +685,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // dense form with an addend: wait for this tile's C in the staging tile
         // (each thread reads exactly the 16-byte units it writes below)
         bool c_in = false;
-        if constexpr (MODE == kDense) {
+        if constexpr (MODE == kDense || MODE == kKGrouped) {
           if (p.C != nullptr) {
             c_in = wait_bar(bar(L::C_FULL), cph, abort_flag, p);
             cph ^= 1;
@@ -632,7 +727,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (pt == 0 && !*abort_flag && T.rows > 0) {
             for (int cc = 0; cc < BN / 32; ++cc)
               if (T.n0 + cc * 32 < p.N)
-                tma_store_3d(&tmD, out_s + cc * (BLOCK_M * 64), T.n0 + cc * 32, T.m0, T.z);
+                tma_store_3d(&tmD, out_s + cc * (BLOCK_M * 64), T.n0 + cc * 32, T.m0, T.zd);
             bulk_commit_group();
           }
         } else if (!*abort_flag) {

@@ -5,8 +5,15 @@
 namespace dgk {
 
 // Which form of the GEMM a launch computes (DeepGEMM, es.news.hada.io/topic?id=19459,
-// "Dense y Grouped GEMM").
-enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+// "Dense y Grouped GEMM"): dense, M-grouped contiguous, M-grouped masked, and
+// the K-grouped form of the MoE weight gradient (groups concatenated along K).
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
+
+// Operand storage (same page, "Interfaz GEMM y restricciones de layout": the
+// nt / nn / tn / tt layouts).  Bit 0: A stored [K][M] ("t"), else [M][K];
+// bit 1: B stored [K][N] ("n"), else [N][K].  A [K][M] operand is MN-major
+// in shared memory, which tcgen05 reads for 8-bit types as well.
+enum Layout : int { kNT = 0, kTT = 1, kNN = 2, kTN = 3 };
 
 constexpr int BLOCK_M = 128;  // rows of A per tile (one tcgen05 M=128 MMA)
 constexpr int BLOCK_K = 128;  // one K group: the granularity of both scale factors
@@ -35,6 +42,7 @@ static_assert(NUM_ISSUERS == 1 || NUM_ISSUERS == 2, "the issuer count must divid
 constexpr int SA_GROUPS = 4;
 constexpr int SA_SLOTS = 4;
 constexpr int MAX_GROUPS_MASKED = 1024;
+constexpr int MAX_GROUPS_KGROUPED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
 constexpr int MAX_SPLIT = 8;  // CTAs per cluster in the K-split form
 
@@ -43,6 +51,7 @@ constexpr unsigned int ST_OK = 0;
 constexpr unsigned int ST_TIMEOUT = 7;      // an mbarrier wait gave up
 constexpr unsigned int ST_MASK_RANGE = 8;   // masked_m[g] outside [0, max_m]; clamped
 constexpr unsigned int ST_EXPERT_RANGE = 9; // m_indices out of range or a block mixes experts
+constexpr unsigned int ST_KS_RANGE = 10;    // ks[g] negative, not a multiple of 128, or past K
 
 // Debug flags (tests of the failure path only).
 constexpr unsigned int DBG_SKIP_PRODUCER = 1u;  // the TMA warp issues nothing
@@ -61,8 +70,9 @@ struct Params {
   const float* sb;             // [G][nb][kb]
   const int32_t* m_indices;    // contiguous: [M_total]
   const int32_t* masked_m;     // masked: [G]
+  const int32_t* ks;           // K-grouped: [G] K rows of each group (multiples of 128)
   uint16_t* D;                 // bf16 output, [M][N] or [G][max_m][N]
-  const uint16_t* C;           // dense only: bf16 addend [M][N] (D = C + A B^T), or null
+  const uint16_t* C;           // dense / K-grouped: bf16 addend shaped like D (D = C + A B), or null
   unsigned int* status;        // device status word
   unsigned long long timeout_ns;
   unsigned int debug_flags;

@@ -286,12 +286,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle: the
+// swizzle atom is 8 K rows of 128 bytes (128 e4m3 values along M or N), K row
+// r of an atom at byte 128 r.  The stride byte offset is the distance between
+// consecutive 8-row groups along K (1024: atoms stacked densely along K), the
+// leading byte offset the distance between consecutive 128-wide atoms along
+// M / N (`lbo` bytes; unused when the operand is one atom wide).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mnmajor(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B e4m3
-// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// (bits 7-9, 10-12 = 0), A and B K-major unless `a_mn` / `b_mn` (bits 15 and
+// 16: the operand is MN-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n, bool a_mn = false,
+                                                      bool b_mn = false) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // -------------------------------------------------------------- cluster ----

@@ -78,6 +78,47 @@ def test_add_c_requires_c(L):
     assert status_of(dg.gemm_fp8_fp8_bf16_nt_add_c, C=P + 8, **a) == 3
 
 
+@pytest.mark.parametrize("name", ["nn", "tn", "tt"])
+def test_layout_argument_errors(L, name):
+    fn = getattr(dg, "gemm_fp8_fp8_bf16_" + name)
+    a_t = name[0] == "t"
+    assert status_of(fn, **_dense(A=None)) == 1
+    assert status_of(fn, **_dense(K=500)) == 2
+    assert status_of(fn, **_dense(N=200)) == 2
+    assert status_of(fn, **_dense(C=P + 8)) == 3
+    assert status_of(fn, **_dense(ld_sa=64)) == 1
+    # A stored [K][M]: a row is M bytes, so M must keep TMA's 16-byte pitch
+    assert (status_of(fn, **_dense(M=120, ld_sa=120)) == 2) == a_t
+    assert status_of(fn, **_dense(M=0)) == 0
+
+
+def _kg(**kw):
+    a = dict(A=P, sa=P, ld_sa=256, B=P, sb=P, D=P, ks=P, num_groups=4, M=256, N=512,
+             K_total=2048)
+    a.update(kw)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(A=None), 1),
+    (dict(ks=None), 1),
+    (dict(num_groups=0), 1),
+    (dict(num_groups=1025), 1),
+    (dict(ld_sa=128), 1),
+    (dict(K_total=500), 2),
+    (dict(K_total=0), 2),
+    (dict(K_total=128 * 513), 2),
+    (dict(M=120, ld_sa=120), 2),
+    (dict(N=200), 2),
+    (dict(C=P + 8), 3),
+    (dict(ks=P + 2), 3),
+    (dict(ld_sa=258), 3),
+    (dict(M=0), 0),
+])
+def test_k_grouped_argument_errors(L, kw, code):
+    assert status_of(dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous, **_kg(**kw)) == code
+
+
 def test_empty_problem_is_a_noop(L):
     # M = 0: nothing to compute, no device needed
     assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(M=0)) == 0
@@ -169,8 +210,14 @@ def test_plan_config_heuristic(L):
     for kind, m, g in ((1, 32768, 4), (2, 256, 8)):
         cfg = dg.plan_config(kind, m, 4096, 7168, g, 152)
         assert cfg["split_k"] == 1 and cfg["smem_bytes"] <= 232448
+    # K-grouped: one tile set per group, no split, MN-major instances
+    cfg = dg.plan_config(3, 4096, 7168, 4 * 4096, 4, 152)
+    assert cfg["split_k"] == 1 and cfg["pair"] == 0 and cfg["smem_bytes"] <= 232448
+    assert cfg["num_tiles"] == 4 * 32 * ((7168 + cfg["block_n"] - 1) // cfg["block_n"])
     with pytest.raises(dg.DGError):
         dg.plan_config(0, 64, 2112, 7000, 1, 152)
+    with pytest.raises(dg.DGError):
+        dg.plan_config(4, 64, 2112, 7168, 1, 152)
 
 
 def test_force_config_hook(L):

@@ -127,6 +127,31 @@ def contiguous_problem(num_groups, N, K, m_lo, m_hi, seed, align=128):
                 M=M, N=N, K=K, G=num_groups, ms=ms)
 
 
+def k_grouped_problem(ks, M, N, seed):
+    """K-grouped (MoE weight-gradient) problem: group g owns ks[g] rows of K
+    (multiples of 128, zeros allowed).  The logical operands a [M, K_all] and
+    b [N, K_all] are quantised like the dense ones (a per row and 128-wide K
+    group, b per 128x128 block) and stored transposed: A [K_all, M],
+    B [K_all, N] (the "tn" storage)."""
+    ks = np.asarray(ks, np.int32)
+    K_all = int(ks.sum())
+    g = _gen(seed)
+    a = torch.randn(M, K_all, generator=g, dtype=torch.float32)
+    b = torch.randn(N, K_all, generator=g, dtype=torch.float32)
+    A, sa = quantize_lhs(a)
+    B, sb = quantize_rhs(b)
+    return dict(A=np.ascontiguousarray(A.numpy().T), sa=sa.numpy(),
+                B=np.ascontiguousarray(B.numpy().T), sb=sb.numpy(), ks=ks, M=M, N=N,
+                K=K_all, G=len(ks))
+
+
+def random_ks(num_groups, k_lo, k_hi, seed):
+    """K rows per group ~ U{k_lo..k_hi} rounded down to whole 128-wide groups."""
+    g = _gen(seed)
+    ks = torch.randint(k_lo, k_hi + 1, (num_groups,), generator=g).numpy()
+    return (ks // 128 * 128).astype(np.int32)
+
+
 def masked_problem(num_groups, max_m, N, K, expected_m, seed, m_lo=1):
     """M-grouped masked problem: masked_m[g] ~ U{m_lo..2*expected_m}, capped at
     max_m.  Rows past masked_m[g] of A hold random codes too."""
@@ -171,6 +196,11 @@ CONFIGS = {
                                nk=GROUPED_NK, seed=1003),
     "grouped_masked": dict(kind="masked", groups=(1, 2, 4, 8), max_m=1024, expected_m=256,
                            nk=GROUPED_NK, seed=1004),
+    # MoE weight gradient: per expert dW [M, N] = dY^T X over its tokens (K);
+    # (M, N) = (4096, 7168) for the fused gate/up projection, (7168, 2048) for
+    # the down projection; tokens per expert ~ U{2048..6144}
+    "k_grouped_wgrad": dict(kind="k_grouped", groups=4, k_range=(2048, 6144),
+                            mn=[(4096, 7168), (7168, 2048)], seed=1006),
     # the activations feeding the dense sweeps: A [M, K] for every M and K above
     "quantize_act": dict(kind="quantize",
                          cases=[(m, k) for m in (64, 128, 4096) for k in
