@@ -63,6 +63,13 @@ class Case:
         kb = K // 128
         N = prob["N"]
         nb = (N + 127) // 128
+        if kind == "k_grouped":
+            # K = all groups' K rows; every group writes a full [M, N] output
+            M, G = prob["M"], prob["G"]
+            self.m_valid = M
+            self.flops = 2.0 * M * N * K
+            self.bytes = K * M + K * N + 4 * M * kb + 4 * nb * kb + 2 * G * M * N
+            return
         if kind == "dense":
             mv, gu = prob["M"], 1
         elif kind == "contiguous":
@@ -75,9 +82,11 @@ class Case:
         self.bytes = mv * K + gu * N * K + 4 * mv * kb + 4 * gu * nb * kb + 2 * mv * N
 
 
-def make_cases(name, only=None, add_c=False):
+def make_cases(name, only=None, add_c=False, layout="nt"):
     cfg = W.CONFIGS[name]
     out = []
+    if layout != "nt":
+        assert cfg["kind"] == "dense", "--layout is for the dense workloads"
     if cfg["kind"] == "quantize":
         for (M, K) in cfg["cases"]:
             out.append(("quantize", lambda M=M, K=K: W.activation_problem(M, K, seed=cfg["seed"]),
@@ -86,6 +95,11 @@ def make_cases(name, only=None, add_c=False):
         for (M, N, K) in cfg["cases"]:
             out.append(("dense", lambda M=M, N=N, K=K: W.dense_problem(M, N, K, seed=cfg["seed"]),
                         f"{M}x{N}x{K}"))
+    elif cfg["kind"] == "k_grouped":
+        for i, (M, N) in enumerate(cfg["mn"]):
+            ks = W.random_ks(cfg["groups"], *cfg["k_range"], seed=cfg["seed"] + i)
+            out.append(("k_grouped", lambda ks=ks, M=M, N=N: W.k_grouped_problem(
+                ks, M, N, seed=cfg["seed"]), f"G{cfg['groups']}x{M}x{N}xK{int(ks.sum())}"))
     elif cfg["kind"] == "contiguous":
         for (N, K) in cfg["nk"]:
             out.append(("contiguous", lambda N=N, K=K: W.contiguous_problem(
@@ -101,14 +115,19 @@ def make_cases(name, only=None, add_c=False):
         out = [out[only]]
     cases = [Case(kind, make(), label) for kind, make, label in out]
     if add_c:
-        assert cfg["kind"] == "dense", "--add-c is for the dense workloads"
+        assert cfg["kind"] in ("dense", "k_grouped"), "--add-c is for the dense and K-grouped workloads"
         for c in cases:
             M, N = c.p["M"], c.p["N"]
+            shape = (c.p["G"], M, N) if c.kind == "k_grouped" else (M, N)
             g = np.random.default_rng(c.p["K"] + M + N)
-            c.p["C"] = (g.standard_normal((M, N)).astype(np.float32).view(np.uint32) >>
+            c.p["C"] = (g.standard_normal(shape).astype(np.float32).view(np.uint32) >>
                         16).astype(np.uint16)   # bf16 bits (truncated N(0,1))
-            c.bytes += 2 * M * N
+            c.bytes += 2 * int(np.prod(shape))
             c.label += "+C"
+    for c in cases:
+        c.layout = layout
+        if layout != "nt":
+            c.label += "+" + layout
     return cases
 
 
@@ -128,6 +147,10 @@ def describe(name):
     if name == "grouped_contiguous":
         return (f"contiguous M-grouped: {cfg['groups']} experts, m_e~U[{cfg['m_range'][0]},"
                 f"{cfg['m_range'][1]}] padded to 128, (N,K) in {cfg['nk']}")
+    if name == "k_grouped_wgrad":
+        return (f"K-grouped tn (MoE weight gradient): {cfg['groups']} experts, tokens per expert "
+                f"K_g~U[{cfg['k_range'][0]},{cfg['k_range'][1]}] rounded down to 128, "
+                f"(M,N) in {cfg['mn']}, A [K,M] and B [K,N] stored MN-major")
     return (f"masked M-grouped: G in {cfg['groups']}, max_m={cfg['max_m']}, "
             f"masked_m~U[1,{2 * cfg['expected_m']}], (N,K) in {cfg['nk']}")
 
@@ -262,10 +285,18 @@ class DeviceCase:
             self.idx = None
             self.inputs = [self.X]
             return
-        self.A, self.sa, self.B, self.sb = dev(p["A"]), dev(p["sa"]), dev(p["B"]), dev(p["sb"])
+        A, B = p["A"], p["B"]
+        if getattr(c, "layout", "nt")[0] == "t":   # the stored forms of the other layouts
+            A = np.ascontiguousarray(A.T)
+        if getattr(c, "layout", "nt")[1] == "n":
+            B = np.ascontiguousarray(B.T)
+        self.A, self.sa, self.B, self.sb = dev(A), dev(p["sa"]), dev(B), dev(p["sb"])
         self.idx = None
         self.C = dev(p["C"].view(np.int16)) if "C" in p else None
-        if c.kind == "dense":
+        if c.kind == "k_grouped":
+            self.idx = dev(p["ks"])
+            self.D = torch.zeros((p["G"], p["M"], p["N"]), dtype=torch.bfloat16, device="cuda")
+        elif c.kind == "dense":
             self.D = torch.zeros((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda")
         elif c.kind == "contiguous":
             self.idx = dev(p["m_indices"])
@@ -281,6 +312,14 @@ class DeviceCase:
         p, dg = self.c.p, self.dg
         if self.c.kind == "quantize":
             dg.quantize_fp8_1x128(self.X, self.D, self.sa, 1, p["M"], p["K"], p["ld_sa"], stream)
+        elif self.c.kind == "k_grouped":
+            dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, self.idx, p["G"],
+                p["M"], p["N"], p["K"], C=self.C, stream=stream)
+        elif self.c.kind == "dense" and self.c.layout != "nt":
+            getattr(dg, "gemm_fp8_fp8_bf16_" + self.c.layout)(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, p["M"], p["N"],
+                p["K"], C=self.C, stream=stream)
         elif self.c.kind == "dense" and self.C is not None:
             dg.gemm_fp8_fp8_bf16_nt_add_c(self.A, self.sa, self.sa.shape[-1], self.B, self.sb,
                                           self.C, self.D, p["M"], p["N"], p["K"], stream)
@@ -334,7 +373,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     _build.build()
     dg.lib()
-    cases = make_cases(args.workload, args.case, add_c=args.add_c)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout)
     dcs = [DeviceCase(c, torch, dg) for c in cases]
     stream = torch.cuda.Stream()
     step_bytes = sum(c.bytes for c in cases)
@@ -422,7 +461,9 @@ def run_ours(args):
                 "peak_source": (f"{src} bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)")}
     desc = describe(args.workload)
     if args.add_c:
-        desc += "; D = C + A B^T with a bf16 addend C read per call"
+        desc += "; D = C + A B with a bf16 addend C read per call"
+    if args.layout != "nt":
+        desc += f"; operands stored as the {args.layout} layout"
     if args.case is not None:
         desc += f" (case {args.case} only: {cases[0].label})"
     big = footprint > 2 * L2_BYTES
@@ -531,6 +572,14 @@ def _oracle_sample(orc, c, rows, ncols, threads):
         return time.perf_counter() - t, r.size * p["K"], p["M"] * p["K"]
     ncols = min(ncols, p["N"])
     nbs = (ncols + 127) // 128
+    if c.kind == "k_grouped":
+        # the same sampled rows of every group's output, through the K-grouped oracle
+        r = np.linspace(0, p["M"] - 1, num=min(rows, p["M"])).astype(np.int64)
+        A, sa = np.ascontiguousarray(p["A"][:, r]), np.ascontiguousarray(p["sa"][:, r])
+        B, sb = np.ascontiguousarray(p["B"][:, :ncols]), np.ascontiguousarray(p["sb"][:nbs])
+        t = time.perf_counter()
+        orc.k_grouped_tn(A, sa, B, sb, p["ks"], nthreads=threads)
+        return time.perf_counter() - t, p["G"] * r.size * ncols, p["G"] * p["M"] * p["N"]
     if c.kind == "dense":
         r = np.linspace(0, p["M"] - 1, num=min(rows, p["M"])).astype(np.int64)
         t = time.perf_counter()
@@ -557,6 +606,11 @@ def _oracle_sample(orc, c, rows, ncols, threads):
         secs += time.perf_counter() - t
         done += r.size * ncols
     return secs, done, c.m_valid * p["N"]
+
+
+def macs_per_output(c):
+    """Multiply-adds per output element (K-grouped: the average group's K)."""
+    return c.p["K"] / c.p["G"] if c.kind == "k_grouped" else c.p["K"]
 
 
 def cpu_baseline(cases):
@@ -589,14 +643,14 @@ def run_reference(args):
     import oracle
     orc = oracle.Oracle()
     cores = len(os.sched_getaffinity(0))
-    cases = make_cases(args.workload, args.case, add_c=args.add_c)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout)
     steps = args.steps if args.steps is not None else 2 * len(cases)
     warm = args.warmup
     budget = 120.0 / max(1, steps + warm)
     s, done, _ = _oracle_sample(orc, cases[0], cores, 128, cores)
     quant = cases[0].kind == "quantize"
     # output-element MACs (quantiser: elements) per second
-    rate = done * (1 if quant else cases[0].p["K"]) / max(s, 1e-6)
+    rate = done * (1 if quant else macs_per_output(cases[0])) / max(s, 1e-6)
     t_full, bytes_sum, wall = 0.0, 0, 0.0
     for i in range(warm + steps):
         c = cases[i % len(cases)]
@@ -605,7 +659,8 @@ def run_reference(args):
             cols = 0
         else:
             rows = min(cores, c.m_valid)
-            cols = int(budget * rate / (rows * c.p["K"]))
+            per_row = macs_per_output(c) * (c.p["G"] if c.kind == "k_grouped" else 1)
+            cols = int(budget * rate / (rows * per_row))
             cols = max(16, min(c.p["N"], cols // 16 * 16))
         secs, done, full = _oracle_sample(orc, c, rows, cols, cores)
         if i >= warm:
@@ -648,6 +703,9 @@ def main(argv=None):
     ap.add_argument("--add-c", action="store_true",
                     help="dense workloads: D = C + A B^T through dg_gemm_fp8_fp8_bf16_nt_add_c "
                          "(a seeded bf16 addend C; its 2*M*N bytes count as read)")
+    ap.add_argument("--layout", choices=["nt", "nn", "tn", "tt"], default="nt",
+                    help="dense workloads: store A and B as this layout names and call "
+                         "dg_gemm_fp8_fp8_bf16_<layout> (the same logical problem)")
     ap.add_argument("--quick", action="store_true",
                     help="skip the per-case cold-L2 detail (profiling runs)")
     args = ap.parse_args(argv)

@@ -12,6 +12,10 @@ const Instance* instances_mn(int* count) {
       InstanceOf<256, 3, false, kDense, 128, false, kTN>::make(),
       InstanceOf<128, 5, false, kDense, 128, false, kTT>::make(),
       InstanceOf<256, 3, false, kDense, 128, false, kTT>::make(),
+      // K split over a cluster (decode shapes; an MN-major A is always a full 128-row box)
+      InstanceOf<128, 6, true, kDense, 128, false, kNN>::make(),
+      InstanceOf<128, 6, true, kDense, 128, false, kTN>::make(),
+      InstanceOf<128, 6, true, kDense, 128, false, kTT>::make(),
       InstanceOf<128, 5, false, kKGrouped, 128, false, kTN>::make(),
       InstanceOf<256, 3, false, kKGrouped, 128, false, kTN>::make(),
   };

@@ -231,9 +231,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
   static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && (BN == 128 || BN == 256)),
                 "the pair form: dense, full A, 128- or 256-wide tiles");
-  static_assert(LAYOUT == kNT || (!SPLIT && !PAIR && AROWS == BLOCK_M && BN % 128 == 0 &&
+  static_assert(LAYOUT == kNT || (!PAIR && AROWS == BLOCK_M && BN % 128 == 0 &&
                                    (MODE == kDense || MODE == kKGrouped)),
-                "MN-major operands: dense or K-grouped, full A, 128-multiple tiles");
+                "MN-major operands: dense (also K-split) or K-grouped, full A, 128-multiple tiles");
   static_assert(MODE != kKGrouped || LAYOUT == kTN, "the K-grouped form is tn");
   constexpr bool A_MN = (LAYOUT & 1) != 0;     // A stored [K][M]
   constexpr bool B_MN = (LAYOUT & 2) != 0;     // B stored [K][N]

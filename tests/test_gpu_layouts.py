@@ -77,6 +77,24 @@ def test_dense_layout_add_c(layout, inplace):
     U.assert_close(got, ORC.gemm_layout(layout, A, p["sa"], B, p["sb"], C), f"{layout} add_c")
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("shape", [(64, 2112, 1024), (128, 4096, 2048), (208, 400, 384)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("split", [2, 3, 5])
+@pytest.mark.parametrize("with_c", [False, True])
+def test_dense_layout_split(layout, shape, split, with_c):
+    """The K split over a cluster with MN-major operands (the decode shapes'
+    configuration), with and without the addend."""
+    M, N, K = shape
+    p = W.dense_problem(M, N, K, seed=M + N + K + split)
+    C = _addend((M, N), seed=M + split) if with_c else None
+    with U.forced_config(128, split, pair=0):
+        got = run_layout(layout, p, C)
+    A, B = _stored(p, layout)
+    U.assert_close(got, ORC.gemm_layout(layout, A, p["sa"], B, p["sb"], C),
+                   f"{layout} {shape} split={split} C={with_c}")
+
+
 def test_layouts_agree_with_nt():
     """All four storages of one logical problem give the same bits (same
     arithmetic, only the operands' shared-memory layout differs)."""
