@@ -188,15 +188,19 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     const Instance& in = tab.p[i];
     if (in.mode != kind || in.layout != layout) continue;
     if (force_bn > 0 && in.block_n != force_bn) continue;
-    // 64-row A tiles serve M <= 64 only, and are the choice there
-    if (in.a_rows < 128 && m_rows > in.a_rows) continue;
+    // 64-row A tiles serve M <= 64 only.  Timed alone (cold L2) they matched
+    // the full-A split, but in the back-to-back decode sweep the sweep took
+    // 186.4 us with them and 168.2 us without, so the heuristic takes them
+    // only under a forced configuration (where they remain the M <= 64 choice).
+    const bool forced = force_bn > 0 || force_split > 0;
+    if (in.a_rows < 128 && (m_rows > in.a_rows || !forced)) continue;
     // The CTA-pair form measured slower than the 128-row form on every shape
     // so far (its promotion, not the MMA, sets the pace): it runs only when
     // forced.
     const int fp = g_force_pair.load();
     if (fp <= 0 && in.pair) continue;
     if (fp == 1 && !in.pair) continue;
-    if (in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
+    if (forced && in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;
     // the K split is for shapes whose output tiles cannot fill the SMs
