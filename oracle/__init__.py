@@ -36,6 +36,15 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
                    own K slice transposed by numpy, with its own scale
                    columns; an empty group gives C (or +0) bit for bit; one
                    group over all of K equals gemm_layout "tn"
+  ue8m0_to_double  pinned: all 256 codes against 2^(e-127) by ldexp and the
+                   format's worked values (0x7F = 1, 0xFF = NaN)
+  decode_sfa/sfb   pinned: scales packed here by a numpy byte view (little-
+                   endian uint8 [..., 4] as int32) decode back to themselves
+  gemm_nt_ue8m0    pinned: equal to gemm_nt with the decoded scales; exact
+                   integer results with power-of-two scales
+  quantize_1x128_ue8m0  pinned: every scale a power of two, the smallest one
+                   >= fp32(amax/448) (tight: half of it is below), codes
+                   within half an e4m3 step of x / s, zero groups
   e4m3_from_float  pinned: torch's float32 -> float8_e4m3fn cast (after
                    clamping to +-448) on every code value, every midpoint
                    between neighbours (ties), saturation and random values
@@ -85,6 +94,11 @@ def _load(path):
                                        _int, _int, _int, _int]
     lib.dg_ref_k_grouped_tn.argtypes = [_u8p, _f32p, _int, _u8p, _f32p, _u16p, _u16p, _int, _int,
                                         _i32p, _int, _int]
+    lib.dg_ref_ue8m0_to_double.argtypes = [ctypes.c_uint8]
+    lib.dg_ref_ue8m0_to_double.restype = ctypes.c_double
+    lib.dg_ref_decode_sfa.argtypes = [_i32p, _f32p, _int, _int]
+    lib.dg_ref_decode_sfb.argtypes = [_i32p, _f32p, _int, _int]
+    lib.dg_ref_quantize_1x128_ue8m0.argtypes = [_u16p, _u8p, _i32p, _int, _int, _int, _int, _int]
     lib.dg_ref_quantize_1x128.argtypes = [_u16p, _u8p, _f32p, _int, _int, _int, _int, _int]
     for f in ("dg_ref_gemm_nt_f64", "dg_ref_gemm_nt", "dg_ref_gemm_nt_rows",
               "dg_ref_grouped_contiguous_rows", "dg_ref_grouped_masked",
@@ -127,6 +141,9 @@ class Oracle:
 
     def e4m3_from_float(self, v):
         return int(self.lib.dg_ref_e4m3_from_float(float(np.float32(v))))
+
+    def ue8m0_to_double(self, code):
+        return self.lib.dg_ref_ue8m0_to_double(int(code) & 0xFF)
 
     def max_threads(self):
         return int(self.lib.dg_ref_max_threads())
@@ -215,6 +232,59 @@ class Oracle:
                                      _p(sb, _f32p), cp, _p(D, _u16p), M, N, _p(ks, _i32p), G,
                                      nthreads)
         return D
+
+    # -- UE8M0 packed scales ------------------------------------------------
+    def decode_sfa(self, sfa, kb):
+        """Packed UE8M0 activation scales [..., ceil(kb/4), ld] int32 ->
+        fp32 [..., kb, ld]."""
+        sfa = _c(sfa, np.int32)
+        *lead, kbp, ld = sfa.shape
+        assert kbp == (kb + 3) // 4
+        flat = sfa.reshape(-1, kbp, ld)
+        out = np.zeros((flat.shape[0], kb, ld), np.float32)
+        for i in range(flat.shape[0]):
+            src = np.ascontiguousarray(flat[i])
+            dst = np.zeros((kb, ld), np.float32)
+            self.lib.dg_ref_decode_sfa(_p(src, _i32p), _p(dst, _f32p), kb, ld)
+            out[i] = dst
+        return out.reshape(*lead, kb, ld)
+
+    def decode_sfb(self, sfb, kb):
+        """Packed UE8M0 block scales [..., nb, ceil(kb/4)] int32 -> fp32
+        [..., nb, kb]."""
+        sfb = _c(sfb, np.int32)
+        *lead, nb, kbp = sfb.shape
+        assert kbp == (kb + 3) // 4
+        flat = sfb.reshape(-1, nb, kbp)
+        out = np.zeros((flat.shape[0], nb, kb), np.float32)
+        for i in range(flat.shape[0]):
+            src = np.ascontiguousarray(flat[i])
+            dst = np.zeros((nb, kb), np.float32)
+            self.lib.dg_ref_decode_sfb(_p(src, _i32p), _p(dst, _f32p), nb, kb)
+            out[i] = dst
+        return out.reshape(*lead, nb, kb)
+
+    def gemm_nt_ue8m0(self, A, sfa, B, sfb, nthreads=0):
+        """The dense GEMM with packed UE8M0 scales: the scales decoded, then
+        the same formula as gemm_nt."""
+        kb = A.shape[1] // 128
+        return self.gemm_nt(A, self.decode_sfa(sfa, kb), B, self.decode_sfb(sfb, kb), nthreads)
+
+    def quantize_1x128_ue8m0(self, X, ld=None, fill=0, nthreads=0):
+        """bf16 bits [G, M, K] (or [M, K]) -> (codes, packed UE8M0 scales
+        [G, ceil(kb/4), ld] int32; bytes of groups past K/128 keep `fill`'s)."""
+        X = _c(X, np.uint16)
+        squeeze = X.ndim == 2
+        if squeeze:
+            X = X[None]
+        G, M, K = X.shape
+        ld = ld or M
+        kbp = (K // 128 + 3) // 4
+        Q = np.zeros((G, M, K), np.uint8)
+        sfa = np.full((G, kbp, ld), fill, np.int32)
+        self.lib.dg_ref_quantize_1x128_ue8m0(_p(X, _u16p), _p(Q, _u8p), _p(sfa, _i32p), G, M, K,
+                                             ld, nthreads)
+        return (Q[0], sfa[0]) if squeeze else (Q, sfa)
 
     def gemm_nt_rows(self, A, sa, B, sb, rows, nthreads=0):
         A = _c(A, np.uint8); B = _c(B, np.uint8)

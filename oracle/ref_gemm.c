@@ -543,3 +543,95 @@ void dg_ref_quantize_1x128(const uint16_t *X, uint8_t *Q, float *sa, int num_gro
         }
     }
 }
+
+/* ------------------------------------------------ UE8M0 packed scales ---- */
+/* The scale format of DeepGEMM's SM100 kernels (es.news.hada.io/topic?id=19459,
+ * "Interfaz GEMM y restricciones de layout": packed UE8M0, four per 32-bit
+ * integer).  UE8M0 is an unsigned 8-bit exponent with bias 127 (the E8M0
+ * scale type of the OCP microscaling formats): code e is 2^(e - 127), and
+ * 0xFF is NaN.  Packing: the four K groups 4i .. 4i+3 of one row share a
+ * 32-bit word, group 4i + j in bits 8j .. 8j+7.
+ *   sfa: [ceil(kb/4)][ld] words, word (i, m) = groups 4i.. of row m
+ *   sfb: [nb][ceil(kb/4)] words, word (b, i) = groups 4i.. of the 128-row block b
+ * The decoders below turn them into the fp32 scales of the main formula
+ * (every UE8M0 value but NaN is exact in fp32, 2^-127 as a subnormal). */
+double dg_ref_ue8m0_to_double(uint8_t e)
+{
+    if (e == 0xFF)
+        return NAN;
+#if DG_REF_MUTANT == 16
+    return ldexp(1.0, (int)e - 128);      /* mutant: bias 128 */
+#else
+    return ldexp(1.0, (int)e - 127);
+#endif
+}
+
+static uint8_t packed_byte(int32_t word, int j)
+{
+#if DG_REF_MUTANT == 17
+    j = 3 - j;                            /* mutant: bytes taken in reverse order */
+#endif
+    return (uint8_t)(((uint32_t)word >> (8 * j)) & 0xFFu);
+}
+
+/* sa[g*ld + m] = scale of (row m, K group g), for g < kb and m < ld */
+void dg_ref_decode_sfa(const int32_t *sfa, float *sa, int kb, int ld)
+{
+    for (int g = 0; g < kb; ++g)
+        for (int m = 0; m < ld; ++m)
+            sa[(size_t)g * ld + m] =
+                (float)dg_ref_ue8m0_to_double(packed_byte(sfa[(size_t)(g / 4) * ld + m], g % 4));
+}
+
+/* sb[b*kb + g] = scale of (block b, K group g) */
+void dg_ref_decode_sfb(const int32_t *sfb, float *sb, int nb, int kb)
+{
+    int kbp = (kb + 3) / 4;
+    for (int b = 0; b < nb; ++b)
+        for (int g = 0; g < kb; ++g)
+            sb[(size_t)b * kb + g] =
+                (float)dg_ref_ue8m0_to_double(packed_byte(sfb[(size_t)b * kbp + g / 4], g % 4));
+}
+
+/* The 1x128 quantiser with UE8M0 scales (the scale rounded up to a power of
+ * two, so that it is exact in the packed format).  In fp32, per row and
+ * K group: a = max(amax, 1e-4); t = a / 448 (one rounding); s = the smallest
+ * power of two >= t; Q = e4m3 (round to nearest even, saturating) of x / s,
+ * exact division by a power of two.  The exponent byte 127 + log2(s) goes to
+ * byte g % 4 of word sfa[g/4][m]; bytes of groups past K/128 are left as they
+ * were.  X, Q as in dg_ref_quantize_1x128; sfa: [G][ceil(kb/4)][ld] words. */
+void dg_ref_quantize_1x128_ue8m0(const uint16_t *X, uint8_t *Q, int32_t *sfa, int num_groups,
+                                 int M, int K, int ld, int nthreads)
+{
+    int kb = K / 128, kbp = (kb + 3) / 4;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int z = 0; z < num_groups; ++z)
+        for (int m = 0; m < M; ++m) {
+            const uint16_t *xr = X + ((size_t)z * M + m) * K;
+            uint8_t *qr = Q + ((size_t)z * M + m) * K;
+            for (int g = 0; g < kb; ++g) {
+                float amax = 0.0f;
+                for (int k = 128 * g; k < 128 * g + 128; ++k) {
+                    float v = fabsf(bf16_bits_to_float(xr[k]));
+                    if (v > amax)
+                        amax = v;
+                }
+                float a = amax > 1e-4f ? amax : 1e-4f;
+                float t = a / 448.0f;
+                int ex;
+                float f = frexpf(t, &ex);         /* t = f * 2^ex, f in [0.5, 1) */
+#if DG_REF_MUTANT == 18
+                int lg = ex - 1;                  /* mutant: rounded down, not up */
+                (void)f;
+#else
+                int lg = (f == 0.5f) ? ex - 1 : ex;   /* log2 of the power-of-two ceiling */
+#endif
+                float inv = ldexpf(1.0f, -lg);
+                for (int k = 128 * g; k < 128 * g + 128; ++k)
+                    qr[k] = dg_ref_e4m3_from_float(bf16_bits_to_float(xr[k]) * inv);
+                uint8_t *word = (uint8_t *)(sfa + ((size_t)z * kbp + g / 4) * ld + m);
+                word[g % 4] = (uint8_t)(127 + lg);   /* little-endian: byte j = bits 8j.. */
+            }
+        }
+}

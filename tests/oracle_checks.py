@@ -513,8 +513,117 @@ def check_quantize_invariants(orc, seed=31):
     assert np.all(Q[0, 1, 128:256] & 0x7F == 0)
 
 
+# ------------------------------------------------- UE8M0 packed scales --
+def _pack_ue8m0(codes):
+    """uint8 exponent codes [..., n] -> int32 words [..., ceil(n/4)], four
+    consecutive codes per word, the first in the lowest byte: a numpy byte
+    view (little-endian), independent of the oracle's shifts."""
+    codes = np.asarray(codes, np.uint8)
+    n = codes.shape[-1]
+    pad = (-n) % 4
+    if pad:
+        codes = np.concatenate([codes, np.zeros(codes.shape[:-1] + (pad,), np.uint8)], axis=-1)
+    return np.ascontiguousarray(codes).view("<i4")
+
+
+def check_ue8m0_codes(orc):
+    """All 256 UE8M0 codes: 2^(e - 127) (numpy's ldexp), 0xFF NaN; and the
+    format's worked values."""
+    for e in range(255):
+        assert orc.ue8m0_to_double(e) == float(np.ldexp(1.0, e - 127)), e
+    assert np.isnan(orc.ue8m0_to_double(255))
+    assert orc.ue8m0_to_double(0x7F) == 1.0 and orc.ue8m0_to_double(0x80) == 2.0
+    assert orc.ue8m0_to_double(0x7E) == 0.5 and orc.ue8m0_to_double(0) == 2.0 ** -127
+
+
+def check_ue8m0_packing(orc, seed=47):
+    """Scales packed by a numpy byte view decode back to themselves, for
+    K group counts that do and do not fill the last word."""
+    rng = np.random.default_rng(seed)
+    for kb in (1, 4, 5, 7, 9):
+        ld, nb = 12, 3
+        ea = rng.integers(100, 150, (kb, ld)).astype(np.uint8)      # [kb, ld] codes
+        eb = rng.integers(100, 150, (nb, kb)).astype(np.uint8)      # [nb, kb]
+        sfa = np.ascontiguousarray(_pack_ue8m0(ea.T).T)             # [ceil(kb/4), ld]
+        sfb = _pack_ue8m0(eb)                                       # [nb, ceil(kb/4)]
+        assert np.array_equal(orc.decode_sfa(sfa, kb), np.ldexp(1.0, ea.astype(int) - 127)), kb
+        assert np.array_equal(orc.decode_sfb(sfb, kb), np.ldexp(1.0, eb.astype(int) - 127)), kb
+
+
+def check_gemm_ue8m0(orc, seed=53):
+    """The packed-scale GEMM equals gemm_nt with the same scales given in
+    fp32, and gives exact integers for integer operands with power-of-two
+    scales whose products cancel."""
+    rng = np.random.default_rng(seed)
+    p = W.dense_problem(9, 200, 640, seed)
+    kb = 5
+    ea = rng.integers(120, 134, (kb, 12)).astype(np.uint8)
+    eb = rng.integers(120, 134, (2, kb)).astype(np.uint8)
+    sfa = np.ascontiguousarray(_pack_ue8m0(ea.T).T)
+    sfb = _pack_ue8m0(eb)
+    sa = np.ldexp(1.0, ea.astype(int) - 127).astype(np.float32)
+    sb = np.ldexp(1.0, eb.astype(int) - 127).astype(np.float32)
+    assert np.array_equal(orc.gemm_nt_ue8m0(p["A"], sfa, p["B"], sfb),
+                          orc.gemm_nt(p["A"], sa, p["B"], sb))
+    ints = _int_codes()
+    M, N, K = 4, 130, 512
+    av = np.where(rng.random((M, K)) < 0.05, rng.integers(-2, 3, (M, K)), 0)
+    bv = np.where(rng.random((N, K)) < 0.05, rng.integers(-2, 3, (N, K)), 0)
+    A = np.vectorize(ints.get)(av).astype(np.uint8)
+    B = np.vectorize(ints.get)(bv).astype(np.uint8)
+    # sa = 2^+k, sb = 2^-k per group: every product of scales is 1
+    k = rng.integers(-5, 6, K // 128)
+    ea = np.repeat((127 + k)[:, None], 4, axis=1).astype(np.uint8)          # [kb, 4]
+    eb = np.repeat((127 - k)[None, :], 2, axis=0).astype(np.uint8)          # [2, kb]
+    sfa = np.ascontiguousarray(_pack_ue8m0(ea.T).T)
+    sfb = _pack_ue8m0(eb)
+    exact = av.astype(np.int64) @ bv.astype(np.int64).T
+    want = _bf16_bits(exact.astype(np.float32))
+    assert np.array_equal(orc.gemm_nt_ue8m0(A, sfa, B, sfb), want)
+
+
+def check_quantize_ue8m0(orc, seed=59):
+    """The UE8M0 quantiser: every scale a power of two s, the smallest one
+    >= fp32(max(amax, 1e-4) / 448) (s / 2 is below it), codes x / s rounded to
+    the nearest e4m3 (within half a step, signs kept), zero and below-floor
+    groups; bytes of groups past K/128 untouched."""
+    rng = np.random.default_rng(seed)
+    G, M, K = 2, 5, 640                        # 5 K groups: the second word half used
+    x = rng.standard_normal((G, M, K))
+    x *= np.repeat(np.exp2(rng.integers(-20, 20, (G, M, K // 128))), 128, axis=-1)
+    x[0, 1, 128:256] = 0.0
+    x[1, 2, :128] = 1e-6 * np.sign(x[1, 2, :128])
+    x[0, 3, :128] = 448.0 * 2.0 ** 5 * np.sign(x[0, 3, :128]) * (np.arange(128) / 127.0)
+    xb = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    bits = xb.view(torch.int16).numpy().view(np.uint16)
+    xf = xb.to(torch.float64).numpy()
+    fill = np.int32(0x5A5A5A5A)
+    Q, sfa = orc.quantize_1x128_ue8m0(bits, ld=8, fill=fill)
+    assert sfa.shape == (G, 2, 8)
+    raw = np.ascontiguousarray(sfa).view(np.uint8).reshape(G, 2, 8, 4)
+    assert np.all(raw[:, 1, :, 1:] == 0x5A), "bytes past K/128 written"
+    assert np.all(sfa[:, :, M:] == fill), "columns past M written"
+    dec = torch_e4m3_values()[Q.astype(np.int64)]
+    for z in range(G):
+        for m in range(M):
+            for g in range(K // 128):
+                e = int(raw[z, g // 4, m, g % 4])
+                s = float(np.ldexp(1.0, e - 127))
+                blk = xf[z, m, g * 128:(g + 1) * 128]
+                a = np.float32(max(float(np.abs(blk).max()), 1e-4))
+                t = float(np.float32(a) / np.float32(448.0))
+                assert s >= t and s / 2 < t, (z, m, g, s, t)
+                u = np.clip(blk / s, -448.0, 448.0)
+                half = np.maximum(np.abs(u) * 2.0 ** -4, 2.0 ** -10) * (1 + 2.0 ** -20)
+                d = dec[z, m, g * 128:(g + 1) * 128]
+                assert np.all(np.abs(d - u) <= half), (z, m, g)
+                assert np.all(d * u >= 0), (z, m, g)
+    assert raw[0, 0, 3, 0] == 127 + 5     # amax = 448 * 2^5 exactly: s = 2^5
+
+
 ALL_CHECKS = [
-    check_gemm_layouts, check_k_grouped,
+    check_gemm_layouts, check_k_grouped, check_ue8m0_codes, check_ue8m0_packing,
+    check_gemm_ue8m0, check_quantize_ue8m0,
     check_e4m3_golden, check_e4m3_all_codes, check_bf16_golden, check_bf16_bruteforce,
     check_bf16_vs_torch_float32, check_gemm_bruteforce, check_gemm_exact_integers,
     check_gemm_identity, check_gemm_linearity_transpose, check_gemm_closed_form,

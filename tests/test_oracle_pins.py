@@ -6,7 +6,9 @@ group, a transposed scale index, a flushed subnormal, truncation instead of
 round-to-nearest-even, a dropped sign, a transposed operand, a dropped scale,
 padding rows computed, the mask ignored, the quantiser's 448 left out,
 truncation in the e4m3 encoder, the addend C dropped, a K-grouped segment
-starting one K group early, A's storage layout ignored) and shows that at least one check
+starting one K group early, A's storage layout ignored, a UE8M0 bias of 128,
+packed UE8M0 bytes read in reverse, the UE8M0 quantiser's scale rounded down)
+and shows that at least one check
 fails for each, so the checks are able to see such mistakes.
 """
 import pytest
@@ -42,6 +44,9 @@ MUTANTS = {
     13: "addend C dropped",
     14: "k-grouped segment starts a K group early",
     15: "A's storage layout ignored",
+    16: "UE8M0 bias 128",
+    17: "UE8M0 bytes unpacked in reverse order",
+    18: "UE8M0 quantiser scale rounded down",
 }
 
 
