@@ -155,6 +155,31 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
                                                    int max_m, int N, int K, int expected_m,
                                                    void* stream);
 
+/* The same GEMMs with packed UE8M0 scales, the scale format of DeepGEMM's SM100
+ * kernels (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
+ * layout": packed UE8M0, four per 32-bit integer).  A UE8M0 code e is the
+ * scale 2^(e - 127) (0xFF: NaN); the four K groups 4i .. 4i+3 share one
+ * int32 word, group 4i + j in bits 8j .. 8j+7.
+ *   sfa  int32 [ceil(K/512)][ld_sfa] (masked: [G][ceil(K/512)][ld_sfa]): word
+ *        (i, m) holds row m's scales of K groups 4i ..; ld_sfa >= rows, a
+ *        multiple of 4; 16-byte aligned
+ *   sfb  int32 [ceil(N/128)][ceil(K/512)] (grouped: [G][ceil(N/128)][ceil(K/512)]):
+ *        word (b, i) holds the 128-row block b's scales of K groups 4i ..
+ * Every other argument, the result's formula and the errors are those of the
+ * fp32-scale entry point of the same name without "_ue8m0"; the scales are
+ * decoded exactly (every UE8M0 value but NaN is an fp32 value).  Bytes of K
+ * groups >= K/128 in the last word are never read. */
+dg_status dg_gemm_fp8_fp8_bf16_nt_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, void* D, int M, int N,
+                                        int K, void* stream);
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
+    const int32_t* m_indices, int M_total, int N, int K, int num_groups, void* stream);
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
+    const int32_t* masked_m, int num_groups, int max_m, int N, int K, int expected_m,
+    void* stream);
+
 /* Per-token 1x128 FP8 quantisation of a bf16 activation matrix: the step that
  * produces the left operand A and its scales sa in the layout the GEMMs above
  * read (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
@@ -179,6 +204,17 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
  * host synchronisation. */
 dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
                                 int ld_sa, void* stream);
+
+/* The quantiser with UE8M0 scales for the "_ue8m0" GEMMs: per row m and K
+ * group g, in fp32, a = max(max_k |X[m,k]|, 1e-4); t = a / 448; s = the
+ * smallest power of two >= t; Q[m,k] = e4m3(X[m,k] / s) (round to nearest
+ * even, saturating; the division by s is exact); the code 127 + log2(s) is
+ * written to byte g % 4 of word sfa[z][g / 4][m] (int32 [num_groups][ceil(K/512)]
+ * [ld_sfa]).  Bytes of K groups >= K/128 and columns m >= M are left as they
+ * were.  Requirements and errors as for dg_quantize_fp8_1x128 (ld_sfa in place
+ * of ld_sa). */
+dg_status dg_quantize_fp8_1x128_ue8m0(const void* X, void* Q, int32_t* sfa, int num_groups,
+                                      int M, int K, int ld_sfa, void* stream);
 
 /* Maximum number of SMs the kernels may use (DeepGEMM set_num_sms / get_num_sms,
  * es.news.hada.io/topic?id=19459, "Utilidades y variables de entorno").

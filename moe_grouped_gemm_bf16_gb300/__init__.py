@@ -15,7 +15,9 @@ import os
 __all__ = [
     "DGError", "lib", "gemm_fp8_fp8_bf16_nt", "gemm_fp8_fp8_bf16_nt_add_c",
     "gemm_fp8_fp8_bf16_nn", "gemm_fp8_fp8_bf16_tn", "gemm_fp8_fp8_bf16_tt",
-    "k_grouped_gemm_fp8_fp8_bf16_tn_contiguous",
+    "k_grouped_gemm_fp8_fp8_bf16_tn_contiguous", "gemm_fp8_fp8_bf16_nt_ue8m0",
+    "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0", "m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0",
+    "quantize_fp8_1x128_ue8m0",
     "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
@@ -36,7 +38,9 @@ STATUS_NAMES = {
 EXPORTED_SYMBOLS = [
     "dg_gemm_fp8_fp8_bf16_nt", "dg_gemm_fp8_fp8_bf16_nt_add_c",
     "dg_gemm_fp8_fp8_bf16_nn", "dg_gemm_fp8_fp8_bf16_tn", "dg_gemm_fp8_fp8_bf16_tt",
-    "dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous",
+    "dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous", "dg_gemm_fp8_fp8_bf16_nt_ue8m0",
+    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0",
+    "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0", "dg_quantize_fp8_1x128_ue8m0",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
     "dg_set_num_sms",
@@ -86,6 +90,12 @@ def lib():
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
         L.dg_quantize_fp8_1x128.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        L.dg_quantize_fp8_1x128_ue8m0.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        L.dg_gemm_fp8_fp8_bf16_nt_ue8m0.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]
+        L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
         L.dg_get_num_sms.argtypes = []
         L.dg_set_num_sms.argtypes = [_i]
         L.dg_get_tma_aligned_size.argtypes = [_i, _i]
@@ -185,6 +195,33 @@ def m_grouped_gemm_fp8_fp8_bf16_nt_masked(A, sa, ld_sa, B, sb, D, masked_m, num_
     _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(
         _ptr(A), _ptr(sa), ld_sa, _ptr(B), _ptr(sb), _ptr(D), _ptr(masked_m), num_groups, max_m,
         N, K, expected_m, _stream(stream)))
+
+
+def gemm_fp8_fp8_bf16_nt_ue8m0(A, sfa, ld_sfa, B, sfb, D, M, N, K, stream=None):
+    """The dense GEMM with packed UE8M0 scales (int32 sfa [ceil(K/512), ld_sfa],
+    sfb [ceil(N/128), ceil(K/512)])."""
+    _check(lib().dg_gemm_fp8_fp8_bf16_nt_ue8m0(_ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb),
+                                               _ptr(D), M, N, K, _stream(stream)))
+
+
+def m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(A, sfa, ld_sfa, B, sfb, D, m_indices, M_total,
+                                                    N, K, num_groups, stream=None):
+    _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
+        _ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb), _ptr(D), _ptr(m_indices), M_total, N, K,
+        num_groups, _stream(stream)))
+
+
+def m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(A, sfa, ld_sfa, B, sfb, D, masked_m, num_groups,
+                                                max_m, N, K, expected_m, stream=None):
+    _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(
+        _ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb), _ptr(D), _ptr(masked_m), num_groups,
+        max_m, N, K, expected_m, _stream(stream)))
+
+
+def quantize_fp8_1x128_ue8m0(X, Q, sfa, num_groups, M, K, ld_sfa, stream=None):
+    """bf16 X [G,M,K] -> e4m3 Q and packed UE8M0 scales sfa int32 [G, ceil(K/512), ld_sfa]."""
+    _check(lib().dg_quantize_fp8_1x128_ue8m0(_ptr(X), _ptr(Q), _ptr(sfa), num_groups, M, K,
+                                             ld_sfa, _stream(stream)))
 
 
 def quantize_fp8_1x128(X, Q, sa, num_groups, M, K, ld_sa, stream=None):

@@ -356,7 +356,8 @@ dg_status encode(CUtensorMap* m, CUtensorMapDataType dt, void* ptr, const uint64
 // unless given).  MN-major operands are read in boxes of 128 x 128 K rows.
 dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, const void* B,
                     void* D, int rows, int zA, int N, int K, int gB, int block_n, int a_rows,
-                    const void* C = nullptr, int layout = dgk::kNT, int zD = 0) {
+                    const void* C = nullptr, int layout = dgk::kNT, int zD = 0,
+                    bool sf_packed = false) {
   const int kb = K / 128;
   if (zD <= 0) zD = zA;
   {
@@ -379,7 +380,17 @@ dg_status make_maps(dgk::Maps* mp, const void* A, const float* sa, int ld_sa, co
                          box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B");
     if (s != DG_OK) return s;
   }
-  {
+  if (sf_packed) {
+    // packed UE8M0 words [z][ceil(kb/4)][ld_sa]: two words per ring slot
+    const int kbp = (kb + 3) / 4;
+    const uint64_t dims[3] = {(uint64_t)ld_sa, (uint64_t)kbp, (uint64_t)zA};
+    const uint64_t str[2] = {(uint64_t)ld_sa * 4, (uint64_t)kbp * ld_sa * 4};
+    const uint32_t box[3] = {128, 2, 1};
+    dg_status s = encode(&mp->sa, CU_TENSOR_MAP_DATA_TYPE_INT32, const_cast<float*>(sa), dims,
+                         str, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         "sfa");
+    if (s != DG_OK) return s;
+  } else {
     const uint64_t dims[3] = {(uint64_t)ld_sa, (uint64_t)kb, (uint64_t)zA};
     const uint64_t str[2] = {(uint64_t)ld_sa * 4, (uint64_t)kb * ld_sa * 4};
     const uint32_t box[3] = {128, (uint32_t)dgk::SA_GROUPS, 1};
@@ -429,7 +440,8 @@ const char* layout_name(int layout) {
 // whole K (K-grouped: the operands' rows, all groups together).
 dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B, const float* sb,
               void* D, const int32_t* idx, int rows, int N, int K, int G, int expected_m,
-              void* stream, const void* C = nullptr, int layout = dgk::kNT) {
+              void* stream, const void* C = nullptr, int layout = dgk::kNT,
+              bool sf_packed = false) {
   read_env_once();
   // -------- validation (host only; nothing is launched on an error) ------
   if (rows < 0 || N < 0 || K < 0)
@@ -491,7 +503,7 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
                 (kind == dgk::kDense || kind == dgk::kKGrouped) ? 1 : G,
                 in.pair ? in.block_n / 2 : in.block_n, in.a_rows, has_c ? C : nullptr, layout,
-                kind == dgk::kKGrouped ? G : 0);
+                kind == dgk::kKGrouped ? G : 0, sf_packed);
   if (s != DG_OK) return s;
 
   dgk::Params p{};
@@ -507,6 +519,8 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.raster_m = kRasterM;
   p.split_k = pl.split;
   p.sb = sb;
+  p.sf_ue8m0 = sf_packed ? 1 : 0;
+  p.kbp = (K / 128 + 3) / 4;
   p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
   p.masked_m = kind == dgk::kMasked ? idx : nullptr;
   p.D = static_cast<uint16_t*>(D);
@@ -574,6 +588,31 @@ dg_status dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(const void* A, const floa
              dgk::kTN);
 }
 
+dg_status dg_gemm_fp8_fp8_bf16_nt_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, void* D, int M, int N,
+                                        int K, void* stream) {
+  return run(dgk::kDense, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, nullptr, M, N, K, 1, M, stream, nullptr,
+             dgk::kNT, true);
+}
+
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
+    const int32_t* m_indices, int M_total, int N, int K, int num_groups, void* stream) {
+  return run(dgk::kContiguous, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, m_indices, M_total, N, K, num_groups,
+             M_total, stream, nullptr, dgk::kNT, true);
+}
+
+dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
+    const int32_t* masked_m, int num_groups, int max_m, int N, int K, int expected_m,
+    void* stream) {
+  return run(dgk::kMasked, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, masked_m, max_m, N, K, num_groups,
+             expected_m, stream, nullptr, dgk::kNT, true);
+}
+
 dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous(const void* A, const float* sa, int ld_sa,
                                                        const void* B, const float* sb, void* D,
                                                        const int32_t* m_indices, int M_total,
@@ -592,8 +631,9 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
              stream);
 }
 
-dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
-                                int ld_sa, void* stream) {
+namespace {
+dg_status quantize(const void* X, void* Q, float* sa, int num_groups, int M, int K, int ld_sa,
+                   void* stream, bool ue8m0) {
   read_env_once();
   if (!X || !Q || !sa) return fail(DG_ERR_INVALID_ARG, "dg_quantize_fp8_1x128: null pointer");
   if (num_groups < 1 || M < 0 || ld_sa < M)
@@ -617,9 +657,20 @@ dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_group
   if (s != DG_OK) return s;
   const cudaError_t e = dgk::launch_quantize_1x128(X, Q, sa, num_groups, M, K, ld_sa,
                                                    sms_in_use(*st),
-                                                   static_cast<cudaStream_t>(stream));
+                                                   static_cast<cudaStream_t>(stream), ue8m0);
   if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
   return ok();
+}
+}  // namespace
+
+dg_status dg_quantize_fp8_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
+                                int ld_sa, void* stream) {
+  return quantize(X, Q, sa, num_groups, M, K, ld_sa, stream, false);
+}
+
+dg_status dg_quantize_fp8_1x128_ue8m0(const void* X, void* Q, int32_t* sfa, int num_groups,
+                                      int M, int K, int ld_sfa, void* stream) {
+  return quantize(X, Q, reinterpret_cast<float*>(sfa), num_groups, M, K, ld_sfa, stream, true);
 }
 
 int dg_get_num_sms(void) {

@@ -47,6 +47,9 @@ struct SmemLayout {
   static constexpr int A_BYTES = AROWS * BLOCK_K;    // e4m3 A slot (16 KB or 8 KB)
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BLOCK_K;
   static constexpr int SA_BYTES = SA_GROUPS * BLOCK_M * 4;  // [SA_GROUPS][128] fp32
+  // packed UE8M0 scales: the two words [2][128] that cover a slot's four K
+  // groups wherever they start
+  static constexpr int SA_PACKED_BYTES = 2 * BLOCK_M * 4;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
   static constexpr int SA_OFF = B_OFF + STAGES * B_BYTES;
@@ -93,6 +96,17 @@ struct Tile {
   int kbeg;   // the tile's K groups [kbeg, kend) (this CTA's slice in the split form)
   int kend;
 };
+
+// UE8M0 scale code -> fp32: 2^(e - 127) (e = 0: the subnormal 2^-127; 0xFF: NaN).
+__device__ __forceinline__ float ue8m0_to_float(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u)
+                : e == 0xFFu ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23);
+}
+
+// Byte g % 4 of a packed UE8M0 word, as a scale.
+__device__ __forceinline__ float ue8m0_scale(uint32_t word, int g) {
+  return ue8m0_to_float((word >> (8 * (g & 3))) & 0xFFu);
+}
 
 __device__ __forceinline__ void raise_status(const Params& p, unsigned int code) {
   atomicCAS(p.status, 0u, code);
@@ -459,9 +473,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // the tensor's end read as zero and are not used)
           if ((g - T.kbeg) % SA_GROUPS == 0) {
             if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
-              mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
-              tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
-                          g, T.z);
+              if (p.sf_ue8m0) {
+                mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_PACKED_BYTES);
+                tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
+                            g >> 2, T.z);
+              } else {
+                mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
+                tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
+                            g, T.z);
+              }
               sa_issued_mask |= 1u << j;
               sa_issued_par = (sa_issued_par & ~(1u << j)) | (jph << j);
             }
@@ -597,7 +617,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int i = pt; i < 3 * tk; i += 32 * NUM_PROMO_WARPS) {
           const int jb = i / tk, gg = i - jb * tk;
           const int nbk = min(blk0 + jb, p.nb - 1);
-          sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + T.kbeg + gg);
+          if (p.sf_ue8m0) {
+            const int gk = T.kbeg + gg;
+            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.sb) +
+                                     (static_cast<size_t>(T.e) * p.nb + nbk) * p.kbp + (gk >> 2));
+            sb_s[i] = ue8m0_scale(w, gk);
+          } else {
+            sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + T.kbeg + gg);
+          }
         }
       }
       named_bar_sync(1, 32 * NUM_PROMO_WARPS);
@@ -623,7 +650,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           tc_fence_after();
           // warps whose TMEM lanes hold no loaded row of A have nothing to add
           if (q * 32 < AROWS) {
-          const float a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
+          // packed: word (g/4 - first group/4) of the slot, byte g % 4
+          const float a_s =
+              p.sf_ue8m0
+                  ? ue8m0_scale(reinterpret_cast<const uint32_t*>(
+                                    sa_ring)[(j * SA_GROUPS + ((g >> 2) - ((g - r) >> 2))) *
+                                                 BLOCK_M + row], g)
+                  : sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
           const float* sbg = sb_s + (g - T.kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for

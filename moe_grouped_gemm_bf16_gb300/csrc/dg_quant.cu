@@ -9,6 +9,11 @@
 //
 // all in fp32 (two divisions per group, one multiply per element).
 //
+// UE8M0 form (the scale format of the SM100 kernels, same page and section:
+// packed UE8M0, four per 32-bit word): the scale is rounded up to a power of
+// two, s = the smallest 2^e >= fp32(a / 448), so x / s is exact; the byte
+// 127 + e goes to byte g % 4 of word [g / 4][m] of the packed scales.
+//
 // Memory-bound (3 bytes per element plus 4 per group), so the instruction
 // count per byte is what to keep low: the grid is (row blocks, K groups,
 // batch), so a thread finds its row and group without a division; 8 threads
@@ -46,6 +51,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+template <bool UE8M0>
 __global__ void __launch_bounds__(QT_THREADS)
 quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float* __restrict__ sa,
                       int M, int K, int kb, int ld_sa) {
@@ -85,7 +91,18 @@ quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float*
 #pragma unroll
     for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float a = fmaxf(amax, 1e-4f);
-    const float factor = __fdiv_rn(448.0f, a);
+    float factor;
+    uint32_t e8 = 0;   // UE8M0: the scale's exponent code
+    if constexpr (UE8M0) {
+      // t = a / 448 is a normal fp32 number here (a >= 1e-4, a <= bf16's largest);
+      // its power-of-two ceiling is 2^(E - 127) when the mantissa is zero, else
+      // 2^(E - 126), E the biased exponent; the factor 1 / s is exact
+      const uint32_t tb = __float_as_uint(__fdiv_rn(a, 448.0f));
+      e8 = ((tb >> 23) & 0xFFu) + ((tb & 0x7FFFFFu) != 0u ? 1u : 0u);
+      factor = __uint_as_float((254u - e8) << 23);
+    } else {
+      factor = __fdiv_rn(448.0f, a);
+    }
     uint4 w;
     w.x = cvt_e4m3x2(x[0] * factor, x[1] * factor) | (cvt_e4m3x2(x[2] * factor, x[3] * factor) << 16);
     w.y = cvt_e4m3x2(x[4] * factor, x[5] * factor) | (cvt_e4m3x2(x[6] * factor, x[7] * factor) << 16);
@@ -95,7 +112,16 @@ quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float*
           (cvt_e4m3x2(x[14] * factor, x[15] * factor) << 16);
     if (m < M) {
       Q[off[j]] = w;
-      if (sub == 0) sa[(static_cast<size_t>(z) * kb + g) * ld_sa + m] = __fdiv_rn(a, 448.0f);
+      if (sub == 0) {
+        if constexpr (UE8M0) {
+          // byte g % 4 of the packed word [z][g / 4][m] (little-endian)
+          const int kbp = (kb + 3) >> 2;
+          reinterpret_cast<uint8_t*>(sa)[((static_cast<size_t>(z) * kbp + (g >> 2)) * ld_sa + m) * 4 +
+                                         (g & 3)] = static_cast<uint8_t>(e8);
+        } else {
+          sa[(static_cast<size_t>(z) * kb + g) * ld_sa + m] = __fdiv_rn(a, 448.0f);
+        }
+      }
     }
   }
 }
@@ -103,11 +129,15 @@ quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float*
 }  // namespace
 
 cudaError_t launch_quantize_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
-                                  int ld_sa, int num_sms, cudaStream_t stream) {
+                                  int ld_sa, int num_sms, cudaStream_t stream, bool ue8m0) {
   (void)num_sms;
   const dim3 grid((M + 32 * QT_ROWS - 1) / (32 * QT_ROWS), K / 128, num_groups);
-  quantize_1x128_kernel<<<grid, QT_THREADS, 0, stream>>>(
-      static_cast<const uint4*>(X), static_cast<uint4*>(Q), sa, M, K, K / 128, ld_sa);
+  if (ue8m0)
+    quantize_1x128_kernel<true><<<grid, QT_THREADS, 0, stream>>>(
+        static_cast<const uint4*>(X), static_cast<uint4*>(Q), sa, M, K, K / 128, ld_sa);
+  else
+    quantize_1x128_kernel<false><<<grid, QT_THREADS, 0, stream>>>(
+        static_cast<const uint4*>(X), static_cast<uint4*>(Q), sa, M, K, K / 128, ld_sa);
   return cudaGetLastError();
 }
 

@@ -119,6 +119,29 @@ def test_k_grouped_argument_errors(L, kw, code):
     assert status_of(dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous, **_kg(**kw)) == code
 
 
+def test_ue8m0_argument_errors(L):
+    d = dict(A=P, sfa=P, ld_sfa=128, B=P, sfb=P, D=P, M=128, N=256, K=512)
+    f = dg.gemm_fp8_fp8_bf16_nt_ue8m0
+    assert status_of(f, **{**d, "sfa": None}) == 1
+    assert status_of(f, **{**d, "ld_sfa": 64}) == 1
+    assert status_of(f, **{**d, "ld_sfa": 130}) == 3
+    assert status_of(f, **{**d, "sfa": P + 4}) == 3
+    assert status_of(f, **{**d, "sfb": P + 2}) == 3
+    assert status_of(f, **{**d, "K": 500}) == 2
+    assert status_of(f, **{**d, "M": 0}) == 0
+    c = dict(A=P, sfa=P, ld_sfa=256, B=P, sfb=P, D=P, m_indices=P, M_total=256, N=256, K=512,
+             num_groups=4)
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0, **{**c, "m_indices": None}) == 1
+    m = dict(A=P, sfa=P, ld_sfa=128, B=P, sfb=P, D=P, masked_m=P, num_groups=4, max_m=128, N=256,
+             K=512, expected_m=64)
+    assert status_of(dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0, **{**m, "num_groups": 1025}) == 1
+    q = dict(X=P, Q=P, sfa=P, num_groups=1, M=128, K=512, ld_sfa=128)
+    assert status_of(dg.quantize_fp8_1x128_ue8m0, **{**q, "sfa": None}) == 1
+    assert status_of(dg.quantize_fp8_1x128_ue8m0, **{**q, "K": 200}) == 2
+    assert status_of(dg.quantize_fp8_1x128_ue8m0, **{**q, "ld_sfa": 130}) == 3
+    assert status_of(dg.quantize_fp8_1x128_ue8m0, **{**q, "M": 0, "ld_sfa": 0}) == 0
+
+
 def test_empty_problem_is_a_noop(L):
     # M = 0: nothing to compute, no device needed
     assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(M=0)) == 0

@@ -1,0 +1,175 @@
+"""Packed UE8M0 scales through the C ABI against the CPU oracle: the dense,
+contiguous and masked GEMMs (every dense instance forced, K splits whose
+slices start inside a packed word), and the UE8M0 quantiser bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_bf16_gb300 as dg
+import oracle
+import workloads as W
+from moe_grouped_gemm_bf16_gb300 import _build
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+ORC = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    global ORC
+    _build.build()
+    ORC = oracle.Oracle()
+    torch.cuda.init()
+
+
+def _exponents(shape, seed, lo=118, hi=136):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi, shape, generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+
+
+def _pack(codes):
+    """uint8 [..., n] -> int32 [..., ceil(n/4)], first code in the lowest byte."""
+    n = codes.shape[-1]
+    pad = (-n) % 4
+    if pad:
+        codes = np.concatenate([codes, np.zeros(codes.shape[:-1] + (pad,), np.uint8)], axis=-1)
+    return np.ascontiguousarray(codes).view("<i4")
+
+
+def _sfa(kb, ld, seed, lead=()):
+    e = _exponents(lead + (ld, kb), seed)                        # [..., ld, kb]
+    return np.ascontiguousarray(np.swapaxes(_pack(e), -1, -2))  # [..., ceil(kb/4), ld]
+
+
+def _sfb(nb, kb, seed, lead=()):
+    return _pack(_exponents(lead + (nb, kb), seed))             # [..., nb, ceil(kb/4)]
+
+
+def dense_ue8m0(M, N, K, seed):
+    ld = W.tma_aligned_ld(M)
+    return dict(A=W.random_codes((M, K), seed), B=W.random_codes((N, K), seed + 1),
+                sfa=_sfa(K // 128, ld, seed + 2), sfb=_sfb((N + 127) // 128, K // 128, seed + 3),
+                M=M, N=N, K=K)
+
+
+def run_dense(p):
+    A, B, sfa, sfb = U.dev(p["A"]), U.dev(p["B"]), U.dev(p["sfa"]), U.dev(p["sfb"])
+    D = torch.full((p["M"], p["N"]), -1, dtype=torch.int16, device="cuda")
+    dg.gemm_fp8_fp8_bf16_nt_ue8m0(A, sfa, sfa.shape[-1], B, sfb, D, p["M"], p["N"], p["K"])
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    return U.to_bits(D)
+
+
+SHAPES = [(64, 256, 640), (128, 2112, 1152), (200, 400, 2048), (333, 528, 896), (1024, 4096, 7168)]
+CFGS = [(0, 0, -1), (128, 1, 0), (256, 1, 0), (128, 3, 0), (128, 5, 0), (256, 3, 0), (128, 7, 0),
+        (256, 1, 1), (128, 1, 1)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("cfg", CFGS, ids=lambda c: f"bn{c[0]}_s{c[1]}_p{c[2]}")
+def test_dense_ue8m0(shape, cfg):
+    M, N, K = shape
+    p = dense_ue8m0(M, N, K, seed=M + N + K)
+    with U.forced_config(cfg[0], cfg[1], pair=cfg[2]):
+        got = run_dense(p)
+    want = ORC.gemm_nt_ue8m0(p["A"], p["sfa"], p["B"], p["sfb"])
+    U.assert_close(got, want, f"ue8m0 {shape} cfg={cfg}")
+
+
+def test_same_scales_same_bits():
+    """Power-of-two scales given packed or as fp32 give the same bits."""
+    M, N, K = 256, 512, 1664
+    p = dense_ue8m0(M, N, K, seed=4)
+    sa = ORC.decode_sfa(p["sfa"], K // 128)
+    sb = ORC.decode_sfb(p["sfb"], K // 128)
+    ref = U.run_dense(dict(A=p["A"], sa=sa, B=p["B"], sb=sb, M=M, N=N, K=K))
+    assert np.array_equal(run_dense(p), ref)
+
+
+def test_contiguous_ue8m0():
+    q = W.contiguous_problem(3, 400, 1152, 100, 300, seed=8)
+    G, K, N = q["G"], q["K"], q["N"]
+    kb, ld = K // 128, q["sa"].shape[-1]
+    sfa, sfb = _sfa(kb, ld, 9), _sfb((N + 127) // 128, kb, 10, lead=(G,))
+    A, B = U.dev(q["A"]), U.dev(q["B"])
+    D = torch.full((q["M"], N), -1, dtype=torch.int16, device="cuda")
+    dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(A, U.dev(sfa), ld, B, U.dev(sfb), D,
+                                                       U.dev(q["m_indices"]), q["M"], N, K, G)
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    want = ORC.grouped_contiguous(q["A"], ORC.decode_sfa(sfa, kb), q["B"],
+                                  ORC.decode_sfb(sfb, kb), q["m_indices"])
+    got = U.to_bits(D)
+    pad = q["m_indices"] < 0
+    assert np.all(got[pad] == 0)
+    U.assert_close(got[~pad], want[~pad], "contiguous ue8m0")
+
+
+def test_masked_ue8m0():
+    q = W.masked_problem(4, 256, 528, 1152, 90, seed=12)
+    G, K, N, max_m = q["G"], q["K"], q["N"], q["max_m"]
+    kb, ld = K // 128, q["sa"].shape[-1]
+    sfa, sfb = _sfa(kb, ld, 13, lead=(G,)), _sfb((N + 127) // 128, kb, 14, lead=(G,))
+    fill = np.uint16(U.W.BF16_SENTINEL).view(np.int16)
+    D = torch.full((G, max_m, N), int(fill), dtype=torch.int16, device="cuda")
+    dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(U.dev(q["A"]), U.dev(sfa), ld, U.dev(q["B"]),
+                                                   U.dev(sfb), D, U.dev(q["masked_m"]), G, max_m,
+                                                   N, K, 90)
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    init = np.full((G, max_m, N), U.W.BF16_SENTINEL, np.uint16)
+    want = ORC.grouped_masked(q["A"], ORC.decode_sfa(sfa, kb), q["B"], ORC.decode_sfb(sfb, kb),
+                              q["masked_m"], init)
+    got = U.to_bits(D)
+    for g in range(G):
+        v = int(q["masked_m"][g])
+        assert np.array_equal(got[g, v:], want[g, v:]), f"rows past masked_m of group {g}"
+        U.assert_close(got[g, :v], want[g, :v], f"masked ue8m0 group {g}")
+
+
+def _act(G, M, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(G, M, K, generator=g)
+    x *= torch.exp2(torch.randint(-30, 30, (G, M, K // 128), generator=g).float()).repeat_interleave(128, -1)
+    if M >= 3:
+        x[0, 0, :128] = 0.0
+        x[0, 1, :128] = 448.0 * 8.0          # amax exactly 448 * 2^3
+        x[0, 2, :128] = 1e-7
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 128, 4), (1, 37, 640, 40), (3, 65, 1152, 68),
+                                   (1, 4096, 7168, 4096)], ids=lambda s: "x".join(map(str, s)))
+def test_quantiser_ue8m0(shape):
+    G, M, K, ld = shape
+    bits = _act(G, M, K, seed=M + K)
+    X = U.dev(bits.view(np.int16))
+    Q = torch.empty((G, M, K), dtype=torch.uint8, device="cuda")
+    fill = 0x5A5A5A5A
+    kbp = (K // 128 + 3) // 4
+    sfa = torch.full((G, kbp, ld), fill, dtype=torch.int32, device="cuda")
+    dg.quantize_fp8_1x128_ue8m0(X, Q, sfa, G, M, K, ld)
+    torch.cuda.synchronize()
+    Qr, sfr = ORC.quantize_1x128_ue8m0(bits, ld=ld, fill=fill)
+    assert np.array_equal(Q.cpu().numpy(), Qr), "codes differ"
+    assert np.array_equal(sfa.cpu().numpy(), sfr), "packed scales differ"
+
+
+def test_quantiser_then_gemm_ue8m0():
+    """GPU UE8M0 quantiser -> GPU UE8M0 GEMM equals the oracle's chain."""
+    M, N, K = 200, 384, 1152
+    bits = _act(1, M, K, seed=6)[0]
+    ld = W.tma_aligned_ld(M)
+    Q = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(((K // 128 + 3) // 4, ld), dtype=torch.int32, device="cuda")
+    dg.quantize_fp8_1x128_ue8m0(U.dev(bits.view(np.int16)), Q, sfa, 1, M, K, ld)
+    B = W.random_codes((N, K), 7)
+    sfb = _sfb((N + 127) // 128, K // 128, 8)
+    D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.gemm_fp8_fp8_bf16_nt_ue8m0(Q, sfa, ld, U.dev(B), U.dev(sfb), D, M, N, K)
+    torch.cuda.synchronize()
+    Qr, sfr = ORC.quantize_1x128_ue8m0(bits, ld=ld)
+    U.assert_close(U.to_bits(D), ORC.gemm_nt_ue8m0(Qr, sfr, B, sfb), "quantise -> gemm ue8m0")
