@@ -82,7 +82,7 @@ class Case:
         self.bytes = mv * K + gu * N * K + 4 * mv * kb + 4 * gu * nb * kb + 2 * mv * N
 
 
-def make_cases(name, only=None, add_c=False, layout="nt"):
+def make_cases(name, only=None, add_c=False, layout="nt", ue8m0=False):
     cfg = W.CONFIGS[name]
     out = []
     if layout != "nt":
@@ -128,6 +128,17 @@ def make_cases(name, only=None, add_c=False, layout="nt"):
         c.layout = layout
         if layout != "nt":
             c.label += "+" + layout
+    if ue8m0:
+        assert cfg["kind"] in ("dense", "contiguous", "masked") and layout == "nt" and not add_c, \
+            "--ue8m0 is for the nt dense / contiguous / masked workloads"
+        for c in cases:
+            # packed UE8M0 scales; the oracle sample reads their fp32 values
+            c.p["sfa"], c.p["sfb"], c.p["sa"], c.p["sb"] = W.ue8m0_packed_scales(c.p["sa"], c.p["sb"])
+            kb, nb = c.p["K"] // 128, (c.p["N"] + 127) // 128
+            gu = (1 if c.kind == "dense" else c.p["G"] if c.kind == "contiguous"
+                  else int((c.p["masked_m"] > 0).sum()))
+            c.bytes -= 3 * (c.m_valid * kb + gu * nb * kb)   # 1 byte per scale, not 4
+            c.label += "+ue8m0"
     return cases
 
 
@@ -290,7 +301,10 @@ class DeviceCase:
             A = np.ascontiguousarray(A.T)
         if getattr(c, "layout", "nt")[1] == "n":
             B = np.ascontiguousarray(B.T)
-        self.A, self.sa, self.B, self.sb = dev(A), dev(p["sa"]), dev(B), dev(p["sb"])
+        self.ue8m0 = "sfa" in p
+        self.A, self.B = dev(A), dev(B)
+        self.sa = dev(p["sfa"]) if self.ue8m0 else dev(p["sa"])
+        self.sb = dev(p["sfb"]) if self.ue8m0 else dev(p["sb"])
         self.idx = None
         self.C = dev(p["C"].view(np.int16)) if "C" in p else None
         if c.kind == "k_grouped":
@@ -320,6 +334,18 @@ class DeviceCase:
             getattr(dg, "gemm_fp8_fp8_bf16_" + self.c.layout)(
                 self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, p["M"], p["N"],
                 p["K"], C=self.C, stream=stream)
+        elif self.ue8m0 and self.c.kind == "dense":
+            dg.gemm_fp8_fp8_bf16_nt_ue8m0(self.A, self.sa, self.sa.shape[-1], self.B, self.sb,
+                                          self.D, p["M"], p["N"], p["K"], stream)
+        elif self.ue8m0 and self.c.kind == "contiguous":
+            dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, self.idx, p["M"],
+                p["N"], p["K"], p["G"], stream)
+        elif self.ue8m0:
+            em = W.CONFIGS["grouped_masked"]["expected_m"]
+            dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(
+                self.A, self.sa, self.sa.shape[-1], self.B, self.sb, self.D, self.idx, p["G"],
+                p["max_m"], p["N"], p["K"], em, stream)
         elif self.c.kind == "dense" and self.C is not None:
             dg.gemm_fp8_fp8_bf16_nt_add_c(self.A, self.sa, self.sa.shape[-1], self.B, self.sb,
                                           self.C, self.D, p["M"], p["N"], p["K"], stream)
@@ -373,7 +399,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     _build.build()
     dg.lib()
-    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout,
+                       ue8m0=args.ue8m0)
     dcs = [DeviceCase(c, torch, dg) for c in cases]
     stream = torch.cuda.Stream()
     step_bytes = sum(c.bytes for c in cases)
@@ -464,6 +491,8 @@ def run_ours(args):
         desc += "; D = C + A B with a bf16 addend C read per call"
     if args.layout != "nt":
         desc += f"; operands stored as the {args.layout} layout"
+    if args.ue8m0:
+        desc += "; packed UE8M0 scales (the fp32 scales rounded up to powers of two)"
     if args.case is not None:
         desc += f" (case {args.case} only: {cases[0].label})"
     big = footprint > 2 * L2_BYTES
@@ -643,7 +672,8 @@ def run_reference(args):
     import oracle
     orc = oracle.Oracle()
     cores = len(os.sched_getaffinity(0))
-    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout)
+    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout,
+                       ue8m0=args.ue8m0)
     steps = args.steps if args.steps is not None else 2 * len(cases)
     warm = args.warmup
     budget = 120.0 / max(1, steps + warm)
@@ -706,6 +736,9 @@ def main(argv=None):
     ap.add_argument("--layout", choices=["nt", "nn", "tn", "tt"], default="nt",
                     help="dense workloads: store A and B as this layout names and call "
                          "dg_gemm_fp8_fp8_bf16_<layout> (the same logical problem)")
+    ap.add_argument("--ue8m0", action="store_true",
+                    help="nt dense / grouped workloads: packed UE8M0 scales through the _ue8m0 "
+                         "entry points (scale bytes counted at 1 byte each)")
     ap.add_argument("--quick", action="store_true",
                     help="skip the per-case cold-L2 detail (profiling runs)")
     args = ap.parse_args(argv)

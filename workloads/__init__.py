@@ -145,6 +145,31 @@ def k_grouped_problem(ks, M, N, seed):
                 K=K_all, G=len(ks))
 
 
+def ue8m0_packed_scales(sa, sb):
+    """Power-of-two stand-ins for a problem's fp32 scales in the packed UE8M0
+    layout (4 K groups per int32, first group in the lowest byte): each scale's
+    exponent code, rounded up to the next power of two.  Returns (sfa, sfb,
+    sa2, sb2), the last two the fp32 values the codes stand for.
+    sa [..., kb, ld] -> sfa [..., ceil(kb/4), ld]; sb [..., nb, kb] -> sfb
+    [..., nb, ceil(kb/4)]."""
+    def codes(x):
+        b = np.ascontiguousarray(x, np.float32).view(np.uint32)
+        e = ((b >> 23) & 0xFF) + ((b & 0x7FFFFF) != 0)
+        return np.where(x > 0, e, 127).astype(np.uint8)
+
+    def pack(c):
+        pad = (-c.shape[-1]) % 4
+        if pad:
+            c = np.concatenate([c, np.zeros(c.shape[:-1] + (pad,), np.uint8)], axis=-1)
+        return np.ascontiguousarray(c).view("<i4")
+
+    ca, cb = codes(sa), codes(sb)
+    sfa = np.ascontiguousarray(np.swapaxes(pack(np.ascontiguousarray(np.swapaxes(ca, -1, -2))), -1, -2))
+    sfb = pack(cb)
+    val = lambda c: np.ldexp(1.0, c.astype(np.int32) - 127).astype(np.float32)
+    return sfa, sfb, val(ca), val(cb)
+
+
 def random_ks(num_groups, k_lo, k_hi, seed):
     """K rows per group ~ U{k_lo..k_hi} rounded down to whole 128-wide groups."""
     g = _gen(seed)
