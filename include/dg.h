@@ -172,6 +172,23 @@ dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked(const void* A, const float* s
 dg_status dg_gemm_fp8_fp8_bf16_nt_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
                                         const void* B, const int32_t* sfb, void* D, int M, int N,
                                         int K, void* stream);
+/* nn / tn / tt and K-grouped with packed UE8M0 scales: the scales are packed
+ * as above (sfa [ceil(K/512)][ld_sfa] per row m, sfb [ceil(N/128)][ceil(K/512)]
+ * per 128-row block of B's n; K-grouped: K = K_total), everything else as in
+ * the fp32-scale entry point of the same name. */
+dg_status dg_gemm_fp8_fp8_bf16_nn_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream);
+dg_status dg_gemm_fp8_fp8_bf16_tn_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream);
+dg_status dg_gemm_fp8_fp8_bf16_tt_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream);
+dg_status dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb,
+    const void* C, void* D, const int32_t* ks, int num_groups, int M, int N, int K_total,
+    void* stream);
 dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
     const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
     const int32_t* m_indices, int M_total, int N, int K, int num_groups, void* stream);

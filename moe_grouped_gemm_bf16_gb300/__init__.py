@@ -17,7 +17,8 @@ __all__ = [
     "gemm_fp8_fp8_bf16_nn", "gemm_fp8_fp8_bf16_tn", "gemm_fp8_fp8_bf16_tt",
     "k_grouped_gemm_fp8_fp8_bf16_tn_contiguous", "gemm_fp8_fp8_bf16_nt_ue8m0",
     "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0", "m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0",
-    "quantize_fp8_1x128_ue8m0",
+    "quantize_fp8_1x128_ue8m0", "gemm_fp8_fp8_bf16_nn_ue8m0", "gemm_fp8_fp8_bf16_tn_ue8m0",
+    "gemm_fp8_fp8_bf16_tt_ue8m0", "k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0",
     "m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
@@ -41,6 +42,8 @@ EXPORTED_SYMBOLS = [
     "dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous", "dg_gemm_fp8_fp8_bf16_nt_ue8m0",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0", "dg_quantize_fp8_1x128_ue8m0",
+    "dg_gemm_fp8_fp8_bf16_nn_ue8m0", "dg_gemm_fp8_fp8_bf16_tn_ue8m0",
+    "dg_gemm_fp8_fp8_bf16_tt_ue8m0", "dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous",
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
     "dg_set_num_sms",
@@ -84,6 +87,11 @@ def lib():
             getattr(L, "dg_gemm_fp8_fp8_bf16_" + name).argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp,
                                                                    _i, _i, _i, _vp]
         L.dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous.argtypes = [
+            _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+        for name in ("nn", "tn", "tt"):
+            getattr(L, f"dg_gemm_fp8_fp8_bf16_{name}_ue8m0").argtypes = [
+                _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp]
+        L.dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
         L.dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous.argtypes = [
             _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
@@ -216,6 +224,30 @@ def m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(A, sfa, ld_sfa, B, sfb, D, maske
     _check(lib().dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(
         _ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb), _ptr(D), _ptr(masked_m), num_groups,
         max_m, N, K, expected_m, _stream(stream)))
+
+
+def _layout_ue8m0(name):
+    def fn(A, sfa, ld_sfa, B, sfb, D, M, N, K, C=None, stream=None):
+        _check(getattr(lib(), f"dg_gemm_fp8_fp8_bf16_{name}_ue8m0")(
+            _ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb), _ptr(C), _ptr(D), M, N, K,
+            _stream(stream)))
+    fn.__name__ = f"gemm_fp8_fp8_bf16_{name}_ue8m0"
+    fn.__doc__ = f"The {name} dense GEMM with packed UE8M0 scales; C optional (may be D)."
+    return fn
+
+
+gemm_fp8_fp8_bf16_nn_ue8m0 = _layout_ue8m0("nn")
+gemm_fp8_fp8_bf16_tn_ue8m0 = _layout_ue8m0("tn")
+gemm_fp8_fp8_bf16_tt_ue8m0 = _layout_ue8m0("tt")
+
+
+def k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0(A, sfa, ld_sfa, B, sfb, D, ks, num_groups, M,
+                                                    N, K_total, C=None, stream=None):
+    """The K-grouped tn GEMM with packed UE8M0 scales (sfa [K_total/512, ld_sfa],
+    sfb [ceil(N/128), K_total/512], int32)."""
+    _check(lib().dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0(
+        _ptr(A), _ptr(sfa), ld_sfa, _ptr(B), _ptr(sfb), _ptr(C), _ptr(D), _ptr(ks), num_groups, M,
+        N, K_total, _stream(stream)))
 
 
 def quantize_fp8_1x128_ue8m0(X, Q, sfa, num_groups, M, K, ld_sfa, stream=None):

@@ -596,6 +596,39 @@ dg_status dg_gemm_fp8_fp8_bf16_nt_ue8m0(const void* A, const int32_t* sfa, int l
              dgk::kNT, true);
 }
 
+dg_status dg_gemm_fp8_fp8_bf16_nn_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream) {
+  return run(dgk::kDense, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, nullptr, M, N, K, 1, M, stream, C, dgk::kNN,
+             true);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_tn_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream) {
+  return run(dgk::kDense, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, nullptr, M, N, K, 1, M, stream, C, dgk::kTN,
+             true);
+}
+
+dg_status dg_gemm_fp8_fp8_bf16_tt_ue8m0(const void* A, const int32_t* sfa, int ld_sfa,
+                                        const void* B, const int32_t* sfb, const void* C, void* D,
+                                        int M, int N, int K, void* stream) {
+  return run(dgk::kDense, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, nullptr, M, N, K, 1, M, stream, C, dgk::kTT,
+             true);
+}
+
+dg_status dg_k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0(
+    const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb,
+    const void* C, void* D, const int32_t* ks, int num_groups, int M, int N, int K_total,
+    void* stream) {
+  return run(dgk::kKGrouped, A, reinterpret_cast<const float*>(sfa), ld_sfa, B,
+             reinterpret_cast<const float*>(sfb), D, ks, M, N, K_total, num_groups, M, stream, C,
+             dgk::kTN, true);
+}
+
 dg_status dg_m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(
     const void* A, const int32_t* sfa, int ld_sfa, const void* B, const int32_t* sfb, void* D,
     const int32_t* m_indices, int M_total, int N, int K, int num_groups, void* stream) {

@@ -173,3 +173,55 @@ def test_quantiser_then_gemm_ue8m0():
     torch.cuda.synchronize()
     Qr, sfr = ORC.quantize_1x128_ue8m0(bits, ld=ld)
     U.assert_close(U.to_bits(D), ORC.gemm_nt_ue8m0(Qr, sfr, B, sfb), "quantise -> gemm ue8m0")
+
+
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt"])
+@pytest.mark.parametrize("shape", [(208, 400, 1152), (512, 2112, 2048)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("split", [0, 3])
+def test_layouts_ue8m0(layout, shape, split):
+    """The nn / tn / tt layouts with packed UE8M0 scales (also K-split, whose
+    slices start inside a packed word), with an addend."""
+    M, N, K = shape
+    p = dense_ue8m0(M, N, K, seed=M + N + K + split)
+    A = np.ascontiguousarray(p["A"].T) if layout[0] == "t" else p["A"]
+    B = np.ascontiguousarray(p["B"].T) if layout[1] == "n" else p["B"]
+    g = torch.Generator().manual_seed(M + N)
+    C = (torch.randn(M, N, generator=g) * 4).to(torch.bfloat16).view(torch.int16)
+    D = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    with U.forced_config(128 if split else 0, split, pair=0 if split else -1):
+        getattr(dg, f"gemm_fp8_fp8_bf16_{layout}_ue8m0")(
+            U.dev(A), U.dev(p["sfa"]), p["sfa"].shape[-1], U.dev(B), U.dev(p["sfb"]), D, M, N, K,
+            C=C.cuda())
+        torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    kb = K // 128
+    want = ORC.gemm_layout(layout, A, ORC.decode_sfa(p["sfa"], kb), B, ORC.decode_sfb(p["sfb"], kb),
+                           C.numpy().view(np.uint16))
+    U.assert_close(U.to_bits(D), want, f"{layout} ue8m0 {shape} split={split}")
+
+
+@pytest.mark.parametrize("ks", [[256, 0, 384, 640], [1152], [128, 512, 0, 896, 384]],
+                         ids=lambda k: "_".join(map(str, k)))
+def test_k_grouped_ue8m0(ks):
+    """K-grouped tn with packed UE8M0 scales: group segments start at any K
+    group, so a ring slot's groups can straddle two packed words."""
+    M, N = 208, 400
+    p = W.k_grouped_problem(ks, M, N, seed=sum(ks))
+    kb, ld = p["K"] // 128, p["sa"].shape[-1]
+    sfa, sfb = _sfa(kb, ld, 21), _sfb((N + 127) // 128, kb, 22)
+    G = len(ks)
+    D = torch.full((G, M, N), -1, dtype=torch.int16, device="cuda")
+    dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0(
+        U.dev(p["A"]), U.dev(sfa), ld, U.dev(p["B"]), U.dev(sfb), D, U.dev(p["ks"]), G, M, N,
+        p["K"])
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    want = ORC.k_grouped_tn(p["A"], ORC.decode_sfa(sfa, kb), p["B"], ORC.decode_sfb(sfb, kb),
+                            p["ks"])
+    got = U.to_bits(D)
+    for g in range(G):
+        if ks[g] == 0:
+            assert not np.any(got[g]), f"empty group {g}"
+        else:
+            U.assert_close(got[g], want[g], f"k-grouped ue8m0 {ks} group {g}")
