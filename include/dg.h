@@ -305,8 +305,10 @@ dg_status dg_debug_force_config(int block_n, int split_k);
 
 /* Test and benchmark hook: -1 (default) lets the heuristic decide whether a
  * dense GEMM runs in the CTA-pair form (256-row tiles computed by a 2-CTA
- * cluster with one shared MMA); 0 never, 1 always (dense only; the grouped
- * forms have no pair kernel, so 1 makes them return DG_ERR_UNSUPPORTED_SHAPE). */
+ * cluster with one shared MMA), and likewise the masked form (256-row blocks
+ * of a group); 0 never, 1 always (the contiguous form and the MN-major layouts
+ * have no pair kernel, so 1 makes them return DG_ERR_UNSUPPORTED_SHAPE).  The
+ * environment variable DG_FORCE_PAIR=0|1 sets the same before the first call. */
 dg_status dg_debug_force_pair(int mode);
 
 #ifdef __cplusplus

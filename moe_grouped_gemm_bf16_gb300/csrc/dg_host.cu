@@ -60,6 +60,8 @@ constexpr int kRasterM = 16;
 void read_env_once() {
   int expected = -1;
   if (!g_force_bn.compare_exchange_strong(expected, 0)) return;
+  // DG_FORCE_PAIR=0|1 (tests and benchmarks only): as dg_debug_force_pair
+  if (const char* s = std::getenv("DG_FORCE_PAIR")) g_force_pair.store(std::atoi(s) ? 1 : 0);
   // DG_FORCE_CONFIG="block_n,split_k" (tests and benchmarks only)
   if (const char* s = std::getenv("DG_FORCE_CONFIG")) {
     int bn = 0, sp = 0;
@@ -220,7 +222,7 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
       }
       long long mblk;
       if (kind == dgk::kMasked || kind == dgk::kKGrouped)
-        mblk = (long long)num_groups * cdiv(m_rows, 128);
+        mblk = (long long)num_groups * cdiv(m_rows, in.pair ? 256 : 128);
       else mblk = cdiv(m_rows, in.pair ? 256 : 128);
       const long long tiles = mblk * cdiv(n, in.block_n);
       const long long c = std::max(1, cap(i, in, in.pair ? 2 : S, smem));
@@ -493,8 +495,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   const Instance& in = table_for(table_id(kind, layout)).p[pl.inst];
   int clusters = pl.clusters;
   if (kind == dgk::kMasked) {
-    const long long ub = (long long)G * cdiv(rows, 128) * cdiv(N, in.block_n);
-    clusters = (int)std::min<long long>(ub, num_sms);
+    // the device decides how many tiles there are: launch for the most that can
+    // exist, at most one resident wave of CTAs (pairs: of 2-CTA clusters)
+    const long long ub = (long long)G * cdiv(rows, in.pair ? 256 : 128) * cdiv(N, in.block_n);
+    const int resident = in.pair ? std::max(1, cap(pl.inst, in, 2, pl.smem)) : num_sms;
+    clusters = (int)std::min<long long>(ub, resident);
   }
   const int grid = std::max(1, clusters) * (in.pair ? 2 : pl.split);
 

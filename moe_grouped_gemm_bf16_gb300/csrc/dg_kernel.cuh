@@ -181,8 +181,12 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
     }
     T.z = lo;
     T.e = lo;
-    T.m0 = (mb - prefix[lo]) * BLOCK_M;
-    T.rows = min(BLOCK_M, mcnt[lo] - T.m0);
+    // pair form: M blocks of 256 rows, CTA `crank` owning 128 of them (the
+    // second half may hold no valid row: it still takes part in the MMA and
+    // stores nothing)
+    T.m0 = PAIR ? (mb - prefix[lo]) * 2 * BLOCK_M + static_cast<int>(crank) * BLOCK_M
+                : (mb - prefix[lo]) * BLOCK_M;
+    T.rows = max(0, min(BLOCK_M, mcnt[lo] - T.m0));
   }
   T.zd = T.z;
   return T;
@@ -243,8 +247,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(!SPLIT || MODE == kDense, "the K split is only used by the dense form");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 64 in [64, 256]");
   static_assert(AROWS == BLOCK_M || (AROWS == 64 && MODE == kDense), "64-row A: dense only");
-  static_assert(!PAIR || (!SPLIT && MODE == kDense && AROWS == BLOCK_M && (BN == 128 || BN == 256)),
-                "the pair form: dense, full A, 128- or 256-wide tiles");
+  static_assert(!PAIR || (!SPLIT && (MODE == kDense || MODE == kMasked) && AROWS == BLOCK_M &&
+                          (BN == 128 || BN == 256)),
+                "the pair form: dense or masked, full A, 128- or 256-wide tiles");
   static_assert(LAYOUT == kNT || (!PAIR && AROWS == BLOCK_M && BN % 128 == 0 &&
                                    (MODE == kDense || MODE == kKGrouped)),
                 "MN-major operands: dense (also K-split) or K-grouped, full A, 128-multiple tiles");
@@ -344,7 +349,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int vc = min(max(v, 0), p.M);
         if (vc != v && blockIdx.x == 0) raise_status(p, ST_MASK_RANGE);
         mcnt[g] = vc;
-        c = (vc + BLOCK_M - 1) / BLOCK_M;
+        c = PAIR ? (vc + 2 * BLOCK_M - 1) / (2 * BLOCK_M) : (vc + BLOCK_M - 1) / BLOCK_M;
       }
       int x = c;
 #pragma unroll

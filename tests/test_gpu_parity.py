@@ -145,6 +145,34 @@ def test_masked_small(cfg):
         U.assert_close(got[g, :v], want[g, :v], f"masked group {g}")
 
 
+MASKED_PAIR_CASES = [
+    # (G, max_m, N, K, masked_m override)
+    (5, 300, 400, 384, [0, 128, 300, 129, 256]),   # empty, one CTA, full, 1 row in the 2nd
+    (4, 200, 528, 1024, [200, 57, 1, 128]),         # max_m not a multiple of 256
+    (3, 1024, 4096, 2048, [512, 1000, 300]),        # several pair blocks per group
+    (8, 512, 4096, 512, [512] * 8),                 # 256-512 pair tiles: several per pair
+]
+
+
+@pytest.mark.parametrize("case", MASKED_PAIR_CASES, ids=lambda c: f"G{c[0]}_m{c[1]}_N{c[2]}_K{c[3]}")
+@pytest.mark.parametrize("bn", [128, 256])
+def test_masked_pair(case, bn):
+    """The masked form over CTA pairs (256-row blocks, each CTA storing only
+    its own valid rows; rows past masked_m untouched, bit for bit)."""
+    G, max_m, N, K, mm = case
+    p = W.masked_problem(G, max_m, N, K, 100, seed=G * 7 + N)
+    p["masked_m"] = np.asarray(mm, np.int32)
+    with U.forced_config(bn, 1, pair=1):
+        got = U.run_masked(p)
+    assert dg.get_device_status() == 0
+    init = np.full(got.shape, W.BF16_SENTINEL, np.uint16)
+    want = ORC.grouped_masked(p["A"], p["sa"], p["B"], p["sb"], p["masked_m"], init)
+    for g in range(G):
+        v = int(mm[g])
+        assert np.all(got[g, v:] == W.BF16_SENTINEL), f"group {g}: rows past masked_m written"
+        U.assert_close(got[g, :v], want[g, :v], f"masked pair group {g} bn={bn}")
+
+
 PAIR_SHAPES = [
     (64, 256, 512),       # the second CTA of the pair has no rows
     (1, 16, 128),
