@@ -208,3 +208,36 @@ def test_k_grouped_bad_ks_reported():
     run_k_grouped(p, ks_dev=bad)
     assert dg.get_device_status() == 10
     assert dg.get_device_status() == 0
+
+
+def test_k_grouped_graph_follows_device_ks():
+    """One captured launch; the group sizes change on the device between
+    replays (the host never reads ks), and each replay computes the new split
+    of the same K rows."""
+    ks1, ks2 = [256, 384, 128], [640, 0, 128]          # both sum to 768
+    M, N = 208, 400
+    p = W.k_grouped_problem(ks1, M, N, seed=31)
+    A, B, sa, sb = U.dev(p["A"]), U.dev(p["B"]), U.dev(p["sa"]), U.dev(p["sb"])
+    ks = U.dev(np.asarray(ks1, np.int32))
+    D = torch.zeros((3, M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    call = lambda: dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous(
+        A, sa, sa.shape[-1], B, sb, D, ks, 3, M, N, p["K"], stream=s.cuda_stream)
+    with torch.cuda.stream(s):
+        call()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call()
+    for kk in (ks1, ks2):
+        ks.copy_(torch.from_numpy(np.asarray(kk, np.int32)))
+        g.replay()
+        torch.cuda.synchronize()
+        want = ORC.k_grouped_tn(p["A"], p["sa"], p["B"], p["sb"], np.asarray(kk, np.int32))
+        got = U.to_bits(D)
+        for gi in range(3):
+            if kk[gi] == 0:
+                assert not np.any(got[gi]), f"ks={kk}: empty group {gi}"
+            else:
+                U.assert_close(got[gi], want[gi], f"graph ks={kk} group {gi}")
+    assert dg.get_device_status() == 0
