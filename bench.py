@@ -663,21 +663,24 @@ def macs_per_output(c):
 
 def cpu_baseline(cases):
     """The oracle as it stands, on this host's cores, on a bounded sample of
-    every case: `cores` whole output rows per case; the time is scaled to the
-    whole case by the ratio of output elements."""
+    every case: 4 x `cores` whole output rows per case (about 10-20 s on a
+    16-core host for the decode sweep); the time is scaled to the whole case by
+    the ratio of output elements."""
     import oracle
     orc = oracle.Oracle()
     cores = len(os.sched_getaffinity(0))
+    rows = 4 * cores
     t_full, wall, total_bytes = 0.0, 0.0, 0
     for c in cases:
-        secs, done, full = _oracle_sample(orc, c, cores, c.p.get("N", 0), cores)
+        secs, done, full = _oracle_sample(orc, c, rows, c.p.get("N", 0), cores)
         wall += secs
         t_full += secs * full / done
         total_bytes += c.bytes
     return {"value": round(total_bytes / t_full / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{cores} whole output rows per case ({len(cases)} cases); time scaled "
-                      f"to the whole case by output elements; {wall:.1f} s wall",
+            "sample": f"{rows} whole output rows per case ({len(cases)} cases; all rows where "
+                      f"a case has fewer); time scaled to the whole case by output elements; "
+                      f"{wall:.1f} s wall",
             "seconds": round(wall, 2)}
 
 
