@@ -788,9 +788,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // Each CTA owns a slice of R = ceil(rows / S) tile rows.  A CTA stages
         // its fp32 partial rows in its (now idle) operand ring, 16-byte unit u
         // of row r at unit u ^ (r & 7) (conflict-free row-per-thread writes),
-        // then one thread sends each owner its slice with a bulk copy into the
-        // owner's receive area (slot [sender rank][row in slice]), completing
-        // bytes on the owner's RED_FULL.  The owner sums the S slices in rank
+        // then one thread sends every other owner its slice with a bulk copy
+        // into that owner's receive area (slot [sender rank][row in slice]),
+        // completing bytes on the owner's RED_FULL; an owner reads its own
+        // slice where it was staged.  The owner sums the S slices in rank
         // order and stores bf16.  READY (S arrivals) tells every CTA that all
         // rings are idle, so receive areas may be written.
         const int R = (T.rows + S - 1) / S;
@@ -812,7 +813,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         fence_proxy_async_smem();  // the bulk copies read what this thread wrote
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         if (pt == 0) {
-          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>(S * own_rows * ROWB));
+          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>((S - 1) * own_rows * ROWB));
           // a signal only: the ring's idleness was already observed through
           // the mbarriers of its last loads and MMAs
           for (int r = 0; r < S; ++r) mbar_arrive_remote_relaxed(bar(L::READY), r);
@@ -822,7 +823,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (pt == 0) {
           for (int o = 0; o < S; ++o) {
             const int rows_o = max(0, min(T.rows, (o + 1) * R) - o * R);
-            if (rows_o == 0) continue;
+            if (rows_o == 0 || o == static_cast<int>(crank)) continue;
             bulk_copy_to_cluster(map_cluster(recv_s + static_cast<uint32_t>(crank) * R * ROWB, o),
                                  stage_s + o * R * ROWB, static_cast<uint32_t>(rows_o * ROWB),
                                  map_cluster(bar(L::RED_FULL), o));
@@ -859,7 +860,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
           for (int r = 0; r < MAX_SPLIT; ++r)
             if (r < S) {
-              const uint4 w = ld_shared_v4(recv_s + static_cast<uint32_t>(r * R * ROWB) + off);
+              // the own slice where it was staged, the others in their receive slots
+              const uint32_t base = r == static_cast<int>(crank)
+                                        ? stage_s + static_cast<uint32_t>(own_r0 * ROWB)
+                                        : recv_s + static_cast<uint32_t>(r * R * ROWB);
+              const uint4 w = ld_shared_v4(base + off);
               v[r] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                                  __uint_as_float(w.w));
             }
