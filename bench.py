@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -183,19 +184,29 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def _code_only(text):
+    """C++ source without its comments and blank space (the sources hold no
+    string literal with a comment marker), so that editing a comment does not
+    count as a change of the kernels."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(workload):
-    """Hash of the sources a workload's kernels and launch choices come from:
+    """Hash of the code a workload's kernels and launch choices come from:
     the quantiser's own files for quantize_act, every other file for the
-    GEMM workloads (the host code, which plans and launches both, in each)."""
+    GEMM workloads (the host code, which plans and launches both, in each);
+    comments and blank space do not count."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_grouped_gemm_bf16_gb300", "csrc")
     quant = workload == "quantize_act"
     for f in sorted(os.listdir(csrc)):
         if f != "dg_host.cu" and f.startswith("dg_quant") != quant:
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,25 +1,31 @@
-// The FP8 fine-grained-scaled GEMM kernel for sm_103a (dense, contiguous and
-// masked M-grouped forms), written for GB300's tensor memory and TMA.
+// The FP8 fine-grained-scaled GEMM kernel for sm_103a, written for GB300's
+// tensor memory and TMA: the dense form, the contiguous and masked M-grouped
+// forms and the K-grouped form, with the optional addend C.
 //
 // What it computes (DeepGEMM, es.news.hada.io/topic?id=19459, "Interfaz GEMM
 // y restricciones de layout" and "Dense y Grouped GEMM"):
-//   D[m,n] = bf16( sum_g (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
-// with A e4m3 [M,K], B e4m3 [N,K] (NT), one fp32 scale per row per 128-wide K
-// group for A (stored K-group-major) and one per 128x128 block for B.
+//   D[m,n] = bf16( C[m,n] + sum_g (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
+// with A e4m3 [M,K] and B e4m3 [N,K] (NT; the LAYOUT parameter also takes
+// them stored [K,M] / [K,N]), one scale per row per 128-wide K group for A
+// (stored K-group-major) and one per 128x128 block for B, fp32 or packed
+// UE8M0 exponents.
 //
-// Structure (one persistent CTA per SM, or one cluster of split_k CTAs):
+// Structure (one persistent CTA per SM, a CTA pair, or one cluster of split_k
+// CTAs per tile):
 //   warp 0      TMA producer: A tile [128 x 128], B tile [BN x 128] into an
-//               S-stage ring; the 128 activation scales of the K group into a
-//               separate ring (they are read later, by the promotion warps).
-//   warp 1      allocates tensor memory; one thread issues 4 tcgen05.mma
-//               (K = 32 each) per K group into one of 2-4 TMEM accumulators,
-//               then commits: the stage goes back to the producer, the
-//               accumulator goes to the promotion warps.
-//   warps 4..11 promotion (two warpgroups): read the group's fp32 partial from TMEM, scale it by
-//               sa[m,g] * sb[n/128,g] and add it into fp32 registers while the
-//               tensor cores already compute the next group (the two-level
-//               accumulation of the pages: DeepSeek's overview
-//               deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
+//               S-stage ring; the activation scales of four K groups at a
+//               time into a separate ring (they are read later, by the
+//               promotion warps).
+//   warps 1-2   warp 1 allocates tensor memory; the two warps take the K groups
+//               in turn, one thread each issuing 4 tcgen05.mma (K = 32 each)
+//               per K group into one of 2-4 TMEM accumulators, then
+//               committing: the stage goes back to the producer, the
+//               accumulator to the promotion warps.
+//   warps 4..11 promotion (two warpgroups): read the group's fp32 partial from
+//               TMEM, scale it by sa[m,g] * sb[n/128,g] and add it into fp32
+//               registers while the tensor cores already compute the next
+//               group (the two-level accumulation of the pages: DeepSeek's
+//               overview deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
 //               Then the bf16 epilogue: a swizzled staging tile stored by TMA,
 //               or, when the K groups are split over a cluster, a fixed-order
 //               reduction of partials pushed through distributed shared memory.
