@@ -55,6 +55,10 @@ template <bool UE8M0>
 __global__ void __launch_bounds__(QT_THREADS)
 quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float* __restrict__ sa,
                       int M, int K, int kb, int ld_sa) {
+  // launched with programmatic dependent launch: the inputs may come from the
+  // previous kernel in the stream, so nothing is read before it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;                                   // 16-element slice of the group
   const int row0 = blockIdx.x * (32 * QT_ROWS) + (threadIdx.x >> 5) * 4 + (lane >> 3);
@@ -131,14 +135,22 @@ quantize_1x128_kernel(const uint4* __restrict__ X, uint4* __restrict__ Q, float*
 cudaError_t launch_quantize_1x128(const void* X, void* Q, float* sa, int num_groups, int M, int K,
                                   int ld_sa, int num_sms, cudaStream_t stream, bool ue8m0) {
   (void)num_sms;
-  const dim3 grid((M + 32 * QT_ROWS - 1) / (32 * QT_ROWS), K / 128, num_groups);
-  if (ue8m0)
-    quantize_1x128_kernel<true><<<grid, QT_THREADS, 0, stream>>>(
-        static_cast<const uint4*>(X), static_cast<uint4*>(Q), sa, M, K, K / 128, ld_sa);
-  else
-    quantize_1x128_kernel<false><<<grid, QT_THREADS, 0, stream>>>(
-        static_cast<const uint4*>(X), static_cast<uint4*>(Q), sa, M, K, K / 128, ld_sa);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((M + 32 * QT_ROWS - 1) / (32 * QT_ROWS), K / 128, num_groups);
+  cfg.blockDim = dim3(QT_THREADS, 1, 1);
+  cfg.stream = stream;
+  // programmatic dependent launch: the blocks may be scheduled while the
+  // previous kernel finishes; they wait for it before reading (griddepcontrol)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const uint4* Xv = static_cast<const uint4*>(X);
+  uint4* Qv = static_cast<uint4*>(Q);
+  return ue8m0 ? cudaLaunchKernelEx(&cfg, quantize_1x128_kernel<true>, Xv, Qv, sa, M, K, K / 128, ld_sa)
+               : cudaLaunchKernelEx(&cfg, quantize_1x128_kernel<false>, Xv, Qv, sa, M, K, K / 128,
+                                    ld_sa);
 }
 
 }  // namespace dgk
