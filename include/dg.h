@@ -3,15 +3,18 @@
  *
  * Every GEMM entry point computes, for the rows it covers,
  *
- *   D[m,n] = bf16( sum over K groups g of (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
+ *   D[m,n] = bf16( [C[m,n] +] sum over K groups g of (A_g . B_g^T)[m,n] * sa[m,g] * sb[n/128,g] )
  *
  * with A e4m3 (OCP "E4M3FN" codes, one byte each), B e4m3, both row-major with
- * K innermost ("NT": LHS not transposed, RHS transposed), g a 128-wide slice of
- * K, one fp32 scale per row per K group for A and one fp32 scale per 128x128
- * block for B, and a bf16 (round-to-nearest-even) output.  This is the GEMM of
- * DeepGEMM (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de
- * layout"; the names follow the original release as listed on
- * deepep.org/zh/deepgemm, "接口设计").
+ * K innermost ("NT": LHS not transposed, RHS transposed) unless the entry point
+ * names another layout, g a 128-wide slice of K, one scale per row per K group
+ * for A and one per 128x128 block for B (fp32, or packed UE8M0 in the "_ue8m0"
+ * entry points), an optional bf16 addend C where the entry point takes one, and
+ * a bf16 (round-to-nearest-even) output.  This is the GEMM of DeepGEMM
+ * (es.news.hada.io/topic?id=19459, "Interfaz GEMM y restricciones de layout";
+ * the original names follow the release as listed on deepep.org/zh/deepgemm,
+ * "接口设计").  The layouts below are those of the NT entry points; the others
+ * state theirs where they are declared.
  *
  * Conventions shared by all entry points
  *  - All tensor arguments are DEVICE pointers owned by the caller; the library
@@ -22,9 +25,9 @@
  *    from the host and never allocates, so it can be captured in a CUDA graph.
  *  - Argument errors are reported by the return value before anything is
  *    launched; dg_last_error_string() gives the detail.  Errors found on the
- *    device (a masked_m out of range, a contiguous block that mixes experts, an
- *    internal wait that timed out) are recorded in a device status word read by
- *    dg_get_device_status().
+ *    device (a masked_m out of range, a contiguous block that mixes experts, a
+ *    bad K-grouped ks entry, an internal wait that timed out) are recorded in a
+ *    device status word read by dg_get_device_status().
  *  - The current CUDA device must be a compute capability 10.3 GPU (GB300).
  *
  * Layouts
