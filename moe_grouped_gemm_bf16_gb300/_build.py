@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdg.so")
 
-SOURCES = ["dg_host.cu", "dg_inst_dense.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_mn.cu", "dg_quant.cu"]
+SOURCES = ["dg_host.cu", "dg_inst_dense.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_mn.cu", "dg_inst_ue8m0.cu", "dg_inst_ue8m0_mn.cu", "dg_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

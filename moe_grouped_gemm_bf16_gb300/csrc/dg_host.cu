@@ -84,19 +84,26 @@ struct Table {
 };
 
 // Instance tables: 0 dense nt, 1 contiguous, 2 masked, 3 MN-major operands
-// (dense nn / tn / tt and the K-grouped form).
-constexpr int kNumTables = 4;
+// (dense nn / tn / tt and the K-grouped form); 4-7 the same with packed UE8M0
+// scales.
+constexpr int kNumTables = 8;
 
-int table_id(int kind, int layout) {
-  return (layout != dgk::kNT || kind == dgk::kKGrouped) ? 3 : kind;
+int table_id(int kind, int layout, bool sfp = false) {
+  return ((layout != dgk::kNT || kind == dgk::kKGrouped) ? 3 : kind) + (sfp ? 4 : 0);
 }
 
 Table table_for(int tid) {
   Table t{nullptr, 0};
-  if (tid == 0) t.p = dgk::instances_dense(&t.n);
-  else if (tid == 1) t.p = dgk::instances_contiguous(&t.n);
-  else if (tid == 2) t.p = dgk::instances_masked(&t.n);
-  else t.p = dgk::instances_mn(&t.n);
+  switch (tid) {
+    case 0: t.p = dgk::instances_dense(&t.n); break;
+    case 1: t.p = dgk::instances_contiguous(&t.n); break;
+    case 2: t.p = dgk::instances_masked(&t.n); break;
+    case 3: t.p = dgk::instances_mn(&t.n); break;
+    case 4: t.p = dgk::instances_dense_ue8m0(&t.n); break;
+    case 5: t.p = dgk::instances_contiguous_ue8m0(&t.n); break;
+    case 6: t.p = dgk::instances_masked_ue8m0(&t.n); break;
+    default: t.p = dgk::instances_mn_ue8m0(&t.n); break;
+  }
   return t;
 }
 
@@ -180,8 +187,8 @@ bool has_split64(const Table& tab) {
 // tile as an average group's K, k / num_groups.
 template <typename Cap>
 Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sms, Cap cap,
-            int force_bn, int force_split, int layout = dgk::kNT) {
-  const Table tab = table_for(table_id(kind, layout));
+            int force_bn, int force_split, int layout = dgk::kNT, bool sfp = false) {
+  const Table tab = table_for(table_id(kind, layout, sfp));
   const int kb = k / 128;
   const int k_model = kind == dgk::kKGrouped ? std::max(128, (k / std::max(1, num_groups)) / 128 * 128) : k;
   Plan best;
@@ -319,7 +326,7 @@ dg_status device_state(DeviceState** out, int* dev_out) {
 int clusters_resident(DeviceState& st, int kind, int inst, const Instance& in, int S, int smem,
                       int num_sms) {
   if (S <= 1) return num_sms;
-  int& slot = st.max_clusters[table_id(kind, in.layout)][inst][S];
+  int& slot = st.max_clusters[table_id(kind, in.layout, in.sfp != 0)][inst][S];
   if (slot == 0) {
     int n = 0;
     if (in.max_clusters(S, kMaxSmem, &n) != cudaSuccess || n <= 0) {
@@ -488,11 +495,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   };
   const int m_plan = kind == dgk::kMasked ? std::max(1, std::min(expected_m, rows)) : rows;
   const Plan pl = choose(kind, m_plan, N, K, G, num_sms, cap, g_force_bn.load(),
-                         g_force_split.load(), layout);
+                         g_force_split.load(), layout, sf_packed);
   if (pl.inst < 0)
     return fail(DG_ERR_UNSUPPORTED_SHAPE, "no kernel configuration for this shape%s",
                 g_force_bn.load() > 0 ? " (DG_FORCE_CONFIG)" : "");
-  const Instance& in = table_for(table_id(kind, layout)).p[pl.inst];
+  const Instance& in = table_for(table_id(kind, layout, sf_packed)).p[pl.inst];
   int clusters = pl.clusters;
   if (kind == dgk::kMasked) {
     // the device decides how many tiles there are: launch for the most that can

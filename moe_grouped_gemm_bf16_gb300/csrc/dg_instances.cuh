@@ -21,6 +21,7 @@ struct Instance {
   int a_rows;      // rows of A per tile loaded by TMA (128, or 64 for M <= 64)
   int pair;        // 1: CTA-pair form (cta_group::2, 256-row tiles over a 2-CTA cluster)
   int layout;      // operand storage (kNT, kNN, kTN, kTT)
+  int sfp;         // 1: packed UE8M0 scales
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
                         cudaStream_t s);
@@ -34,6 +35,11 @@ const Instance* instances_contiguous(int* count);
 const Instance* instances_masked(int* count);
 // dense nn / tn / tt and the K-grouped tn form (MN-major operands)
 const Instance* instances_mn(int* count);
+// the same tables with packed UE8M0 scales
+const Instance* instances_dense_ue8m0(int* count);
+const Instance* instances_contiguous_ue8m0(int* count);
+const Instance* instances_masked_ue8m0(int* count);
+const Instance* instances_mn_ue8m0(int* count);
 
 }  // namespace dgk
 
@@ -43,9 +49,10 @@ const Instance* instances_mn(int* count);
 namespace dgk {
 
 template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false,
-          int LAYOUT = kNT>
+          int LAYOUT = kNT, bool SFP = false>
 struct InstanceOf {
-  static constexpr auto kernel = fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS, PAIR, LAYOUT>;
+  static constexpr auto kernel =
+      fp8_gemm_kernel<BN, STAGES, SPLIT, MODE, AROWS, PAIR, LAYOUT, SFP>;
 
   static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
                             cudaStream_t s) {
@@ -93,7 +100,7 @@ struct InstanceOf {
   }
 
   static Instance make() {
-    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0, LAYOUT,
+    return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0, LAYOUT, SFP ? 1 : 0,
                     SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF + 1024, &launch,
                     &set_smem, &max_clusters};
   }

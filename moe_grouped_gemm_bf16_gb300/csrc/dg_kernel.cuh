@@ -244,8 +244,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 namespace dgk {
 
+// SFP: the scales are packed UE8M0 exponents (a separate instance, so that the
+// fp32-scale kernels carry no decode in their promotion loop).
 template <int BN, int STAGES, bool SPLIT, int MODE, int AROWS = BLOCK_M, bool PAIR = false,
-          int LAYOUT = kNT>
+          int LAYOUT = kNT, bool SFP = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
@@ -484,7 +486,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // the tensor's end read as zero and are not used)
           if ((g - T.kbeg) % SA_GROUPS == 0) {
             if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
-              if (p.sf_ue8m0) {
+              if constexpr (SFP) {
                 mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_PACKED_BYTES);
                 tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
                             g >> 2, T.z);
@@ -628,7 +630,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int i = pt; i < 3 * tk; i += 32 * NUM_PROMO_WARPS) {
           const int jb = i / tk, gg = i - jb * tk;
           const int nbk = min(blk0 + jb, p.nb - 1);
-          if (p.sf_ue8m0) {
+          if constexpr (SFP) {
             const int gk = T.kbeg + gg;
             const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.sb) +
                                      (static_cast<size_t>(T.e) * p.nb + nbk) * p.kbp + (gk >> 2));
@@ -662,12 +664,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // warps whose TMEM lanes hold no loaded row of A have nothing to add
           if (q * 32 < AROWS) {
           // packed: word (g/4 - first group/4) of the slot, byte g % 4
-          const float a_s =
-              p.sf_ue8m0
-                  ? ue8m0_scale(reinterpret_cast<const uint32_t*>(
-                                    sa_ring)[(j * SA_GROUPS + ((g >> 2) - ((g - r) >> 2))) *
-                                                 BLOCK_M + row], g)
-                  : sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
+          float a_s;
+          if constexpr (SFP)
+            a_s = ue8m0_scale(reinterpret_cast<const uint32_t*>(
+                                  sa_ring)[(j * SA_GROUPS + ((g >> 2) - ((g - r) >> 2))) *
+                                               BLOCK_M + row], g);
+          else
+            a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
           const float* sbg = sb_s + (g - T.kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
