@@ -531,7 +531,6 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.raster_m = kRasterM;
   p.split_k = pl.split;
   p.sb = sb;
-  p.sf_ue8m0 = sf_packed ? 1 : 0;
   p.kbp = (K / 128 + 3) / 4;
   p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
   p.masked_m = kind == dgk::kMasked ? idx : nullptr;

@@ -67,8 +67,8 @@ struct Params {
   int num_n_blocks;  // ceil(N / BLOCK_N)
   int raster_m;      // M blocks per raster band
   int split_k;       // CTAs per cluster, each taking a slice of the K groups
-  const float* sb;             // [G][nb][kb] fp32, or [G][nb][kbp] packed UE8M0 words
-  int sf_ue8m0;                // 1: sa and sb hold packed UE8M0 exponents (4 K groups per word)
+  const float* sb;             // [G][nb][kb] fp32, or [G][nb][kbp] packed UE8M0 words (the
+                               // instance's SFP parameter says which)
   int kbp;                     // ceil(kb / 4): packed words per row of scales
   const int32_t* m_indices;    // contiguous: [M_total]
   const int32_t* masked_m;     // masked: [G]
