@@ -142,6 +142,30 @@ def test_ue8m0_argument_errors(L):
     assert status_of(dg.quantize_fp8_1x128_ue8m0, **{**q, "M": 0, "ld_sfa": 0}) == 0
 
 
+@pytest.mark.parametrize("name", ["nn", "tn", "tt"])
+def test_layout_ue8m0_argument_errors(L, name):
+    fn = getattr(dg, f"gemm_fp8_fp8_bf16_{name}_ue8m0")
+    d = dict(A=P, sfa=P, ld_sfa=128, B=P, sfb=P, D=P, M=128, N=256, K=512)
+    assert status_of(fn, **{**d, "sfa": None}) == 1
+    assert status_of(fn, **{**d, "K": 500}) == 2
+    assert status_of(fn, **{**d, "ld_sfa": 130}) == 3
+    assert status_of(fn, **{**d, "C": P + 8}) == 3
+    assert (status_of(fn, **{**d, "M": 120, "ld_sfa": 120}) == 2) == (name[0] == "t")
+    assert status_of(fn, **{**d, "M": 0}) == 0
+
+
+def test_k_grouped_ue8m0_argument_errors(L):
+    f = dg.k_grouped_gemm_fp8_fp8_bf16_tn_contiguous_ue8m0
+    d = dict(A=P, sfa=P, ld_sfa=256, B=P, sfb=P, D=P, ks=P, num_groups=4, M=256, N=512,
+             K_total=2048)
+    assert status_of(f, **{**d, "ks": None}) == 1
+    assert status_of(f, **{**d, "num_groups": 1025}) == 1
+    assert status_of(f, **{**d, "K_total": 500}) == 2
+    assert status_of(f, **{**d, "M": 120, "ld_sfa": 120}) == 2
+    assert status_of(f, **{**d, "sfb": P + 2}) == 3
+    assert status_of(f, **{**d, "M": 0}) == 0
+
+
 def test_empty_problem_is_a_noop(L):
     # M = 0: nothing to compute, no device needed
     assert status_of(dg.gemm_fp8_fp8_bf16_nt, **_dense(M=0)) == 0
