@@ -46,3 +46,23 @@ def test_case_algorithmic_counts():
     Kt = int(ks.sum())
     assert k.flops == 2.0 * M * N * Kt
     assert k.bytes == Kt * M + Kt * N + 4 * M * (Kt // 128) + 4 * nb * (Kt // 128) + 2 * 3 * M * N
+
+
+def test_ue8m0_stand_in_scales():
+    """The bench's packed UE8M0 stand-ins decode (through the oracle) to the
+    fp32 values the generator reports, each the power-of-two ceiling of the
+    original scale."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    import workloads as W
+    p = W.dense_problem(40, 300, 640, seed=3)
+    sfa, sfb, sa2, sb2 = W.ue8m0_packed_scales(p["sa"], p["sb"])
+    orc = oracle.Oracle()
+    kb = 640 // 128
+    assert np.array_equal(orc.decode_sfa(sfa, kb), sa2)
+    assert np.array_equal(orc.decode_sfb(sfb, kb), sb2)
+    live = p["sa"][:, :40]
+    assert np.all(sa2[:, :40] >= live) and np.all(sa2[:, :40] < 2 * live)
+    assert np.all(sb2 >= p["sb"]) and np.all(sb2 < 2 * p["sb"])
+    assert np.all(np.log2(sb2) == np.round(np.log2(sb2)))
