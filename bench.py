@@ -2,19 +2,30 @@
 """Benchmark of the FP8 fine-grained-scaled GEMM library on GB300.
 
 `python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                 [--workload dense_decode|dense_prefill|grouped_contiguous|grouped_masked]
+                 [--workload all|dense_tiny|dense_decode|dense_prefill|
+                             grouped_contiguous|grouped_masked|...]
                  [--case I]`
 
-Prints one JSON line.  A step is one pass of the GEMM over every case of the
-workload (default: the dense decode sweep, M in {64, 128} x six (N, K) pairs of
-the DeepSeek-V3/R1 inference shapes), with all inputs resident in HBM and the
-step captured once in a CUDA graph.  `value` is algorithmic HBM bytes per
-second (GB/s) over the K timed steps; `e2e` is the same metric through the C
-ABI with the inputs copied from pinned host memory and the outputs copied back
-inside every step.
+Prints one JSON line.  By default (`--workload all`) every workload of the
+method's benchmark runs in one process: the dense tiny case, the dense decode
+sweep (M in {64, 128}), the dense prefill sweep (M = 4096) over six (N, K)
+pairs of the DeepSeek-V3/R1 inference shapes, the contiguous M-grouped MoE
+GEMM and the masked M-grouped MoE GEMM.  A step of a workload is one pass of
+the GEMM over every case of that workload, with all inputs resident in HBM and
+the step captured once in a CUDA graph; each workload's K steps are timed with
+CUDA events on the launching stream.
+
+The line's headline (`value`, `unit`, `roofline`, `cpu_baseline`, `e2e`) is the
+largest of the workloads, the contiguous MoE GEMM (4 experts, about 32768
+rows), in TFLOP/s; `per_config` holds the same record for every workload:
+GB/s and TFLOP/s, the fraction of the roofline of each case's binding roof
+(the ideal time of a case is the larger of bytes / HBM peak and FLOPs / FP8
+peak), the same against the nominal 8 TB/s and 4.5 PFLOP/s, the CPU oracle on
+a bounded sample and the end-to-end figure through the C ABI with the inputs
+copied from pinned host memory and the outputs copied back inside every step.
 
 `--impl reference` times the CPU oracle (the plain C reference) on this
-machine's host cores instead, on a bounded sample of the same workload.
+machine's host cores instead, on a bounded sample of the headline workload.
 
 Under torchrun (N > 1) every rank runs the whole workload on its own GPU
 (replicas, no collective on the data path); timing is the max over ranks.
@@ -41,8 +52,14 @@ import workloads as W  # noqa: E402
 METRIC = "FP8 block-scaled GEMM TFLOPS & HBM GB/s, % of GB300 FP8/HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0       # GB300 HBM3e, nominal
+NOMINAL_FP8_TFLOPS = 4500.0    # GB300 dense FP8 tensor rate, nominal
 L2_BYTES = 129 * 1024 * 1024
-HBM_BOUND = ("dense_decode", "quantize_act")
+#: the workloads of the default run, in the order they are timed
+ALL_WORKLOADS = ("dense_tiny", "dense_decode", "dense_prefill", "grouped_contiguous",
+                 "grouped_masked")
+#: the headline: the largest single-GPU workload
+HEADLINE = "grouped_contiguous"
 
 
 # ------------------------------------------------------------- workloads ---
@@ -157,13 +174,13 @@ def describe(name):
     if name == "dense_tiny":
         return "dense M=128, N=256, K=512"
     if name == "grouped_contiguous":
-        return (f"contiguous M-grouped: {cfg['groups']} experts, m_e~U[{cfg['m_range'][0]},"
+        return (f"contiguous M-grouped MoE GEMM: {cfg['groups']} experts, m_e~U[{cfg['m_range'][0]},"
                 f"{cfg['m_range'][1]}] padded to 128, (N,K) in {cfg['nk']}")
     if name == "k_grouped_wgrad":
         return (f"K-grouped tn (MoE weight gradient): {cfg['groups']} experts, tokens per expert "
                 f"K_g~U[{cfg['k_range'][0]},{cfg['k_range'][1]}] rounded down to 128, "
                 f"(M,N) in {cfg['mn']}, A [K,M] and B [K,N] stored MN-major")
-    return (f"masked M-grouped: G in {cfg['groups']}, max_m={cfg['max_m']}, "
+    return (f"masked M-grouped MoE GEMM: G in {cfg['groups']}, max_m={cfg['max_m']}, "
             f"masked_m~U[1,{2 * cfg['expected_m']}], (N,K) in {cfg['nk']}")
 
 
@@ -174,6 +191,7 @@ def data_desc(name):
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as fh:
@@ -182,6 +200,27 @@ def measured_peaks():
             d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class Peaks:
+    """Roofline denominators: the measured HBM copy bandwidth and the dense FP8
+    tensor rate taken as 2x the measured bf16 cuBLAS burst (the nominal
+    fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)."""
+
+    def __init__(self):
+        self.hbm, bf16, _, self.src = measured_peaks()
+        self.fp8 = 2.0 * bf16
+
+    def ideal_s(self, c, hbm=None, fp8=None):
+        """Seconds of case c at its binding roof."""
+        return max(c.bytes / ((hbm or self.hbm) * 1e9), c.flops / ((fp8 or self.fp8) * 1e12))
+
+    def bound(self, cases):
+        """The roof that binds a whole step: the one its cases spend more
+        ideal time against."""
+        t_mem = sum(c.bytes for c in cases) / (self.hbm * 1e9)
+        t_cmp = sum(c.flops for c in cases) / (self.fp8 * 1e12)
+        return "hbm" if t_mem >= t_cmp else "tensor"
 
 
 def _code_only(text):
@@ -230,6 +269,42 @@ def recorded_traffic(workload):
     return None
 
 
+def roofline(name, cases, seconds, peaks, launches):
+    """The roofline record of one workload's step: achieved rate against the
+    binding roof of the step, the fraction of each case's own binding roof
+    (sum of the cases' ideal times over the measured time) and the same
+    against the nominal peaks."""
+    bound = peaks.bound(cases)
+    B = sum(c.bytes for c in cases)
+    F = sum(c.flops for c in cases)
+    ideal = sum(peaks.ideal_s(c) for c in cases)
+    ideal_nom = sum(peaks.ideal_s(c, NOMINAL_HBM_GBS, NOMINAL_FP8_TFLOPS) for c in cases)
+    per_launch_s = seconds / max(1, launches)
+    if bound == "hbm":
+        achieved = B / launches / per_launch_s / 1e9
+        peak, unit, nominal = peaks.hbm, "GB/s", NOMINAL_HBM_GBS
+        src = ("measured HBM copy, MEASURED_PEAKS.json hbm_gbs" if peaks.src == "measured"
+               else "fallback 6.8 TB/s")
+    else:
+        achieved = F / launches / per_launch_s / 1e12
+        peak, unit, nominal = peaks.fp8, "TFLOP/s", NOMINAL_FP8_TFLOPS
+        src = f"{peaks.src} bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)"
+    n_hbm = sum(1 for c in cases if c.bytes / peaks.hbm / 1e9 >= c.flops / peaks.fp8 / 1e12)
+    return {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "frac_binding": round(ideal / seconds, 4),
+            "frac_nominal": round(achieved / nominal, 4),
+            "frac_binding_nominal": round(ideal_nom / seconds, 4),
+            "cases_hbm_bound": n_hbm, "cases_tensor_bound": len(cases) - n_hbm,
+            "traffic": recorded_traffic(name), "peak_source": src}
+
+
+def value_of(cases, seconds, unit):
+    if unit == "GB/s":
+        return sum(c.bytes for c in cases) / seconds / 1e9
+    return sum(c.flops for c in cases) / seconds / 1e12
+
+
 # ---------------------------------------------------------------- clocks ---
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -248,7 +323,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -258,7 +333,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -270,15 +345,26 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+        return self.lines
+
+    @staticmethod
+    def summarize(lines, t0=None, t1=None):
+        """Median SM clock, max clock and the throttle reasons seen in the
+        samples taken in [t0, t1] (all samples when not given)."""
+        if not lines:
+            return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, smax, reasons = [], [], set()
-        for ln in self.lines:
+        sm, smax, power, reasons = [], [], [], set()
+        for t, ln in lines:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 7:
                 continue
             try:
                 sm.append(float(parts[0]))
                 smax.append(float(parts[1]))
+                power.append(float(parts[2]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[3:7]):
@@ -287,7 +373,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 # --------------------------------------------------------------- GPU arm ---
@@ -332,6 +419,10 @@ class DeviceCase:
                                  device="cuda")
         self.inputs = [self.A, self.sa, self.B, self.sb] + (
             [self.idx] if self.idx is not None else []) + ([self.C] if self.C is not None else [])
+
+    def footprint(self):
+        return sum(t.numel() * t.element_size() for t in self.inputs) + \
+            self.D.numel() * self.D.element_size()
 
     def call(self, stream):
         p, dg = self.c.p, self.dg
@@ -400,6 +491,70 @@ def barrier(pg):
         pg.barrier()
 
 
+class Workload:
+    """One workload on the device: its cases, their resident tensors and the
+    CUDA graph of one step (every case once)."""
+
+    def __init__(self, name, args, torch, dg, stream):
+        self.name = name
+        self.cases = make_cases(name, args.case, add_c=args.add_c, layout=args.layout,
+                                ue8m0=args.ue8m0)
+        self.dcs = [DeviceCase(c, torch, dg) for c in self.cases]
+        self.footprint = sum(d.footprint() for d in self.dcs)
+        with torch.cuda.stream(stream):
+            # eager warm-up (device set-up, occupancy queries), then graph capture
+            for _ in range(2):
+                for d in self.dcs:
+                    d.call(stream.cuda_stream)
+            stream.synchronize()
+            if dg.get_device_status(stream.cuda_stream) != 0:
+                raise RuntimeError(f"{name}: device status set during warm-up")
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                for d in self.dcs:
+                    d.call(stream.cuda_stream)
+        self.launches = len(self.dcs)
+        self.ms = None
+
+    def describe(self, args):
+        desc = describe(self.name)
+        if args.add_c:
+            desc += "; D = C + A B with a bf16 addend C read per call"
+        if args.layout != "nt":
+            desc += f"; operands stored as the {args.layout} layout"
+        if args.ue8m0:
+            desc += "; packed UE8M0 scales (the fp32 scales rounded up to powers of two)"
+        if args.case is not None:
+            desc += f" (case {args.case} only: {self.cases[0].label})"
+        return desc
+
+    def l2_note(self):
+        if self.footprint > 2 * L2_BYTES:
+            return (f"inputs larger than L2: step footprint {self.footprint / 1e6:.0f} MB vs "
+                    f"129 MB L2; each case's buffers are evicted by the other cases before it "
+                    f"runs again")
+        return (f"step footprint {self.footprint / 1e6:.0f} MB: NOT larger than L2, repeats may "
+                f"hit L2")
+
+
+def time_steps(w, torch, stream, steps, pg):
+    """K graph replays of a workload between CUDA events on the launching
+    stream, with a barrier and a device synchronisation on both sides; the
+    max over ranks of the elapsed milliseconds."""
+    barrier(pg)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            w.graph.replay()
+        t1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(pg)
+    return max_over_ranks(pg, t0.elapsed_time(t1))
+
+
 def run_ours(args):
     import torch
 
@@ -410,132 +565,115 @@ def run_ours(args):
     torch.cuda.set_device(local)
     _build.build()
     dg.lib()
-    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout,
-                       ue8m0=args.ue8m0)
-    dcs = [DeviceCase(c, torch, dg) for c in cases]
+    names = ALL_WORKLOADS if args.workload == "all" else (args.workload,)
+    head = HEADLINE if args.workload == "all" else args.workload
+    peaks = Peaks()
     stream = torch.cuda.Stream()
-    step_bytes = sum(c.bytes for c in cases)
-    step_flops = sum(c.flops for c in cases)
-    footprint = sum(sum(t.numel() * t.element_size() for t in d.inputs) +
-                    d.D.numel() * d.D.element_size() for d in dcs)
+    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
 
+    t_gen = time.perf_counter()
+    wls = []
+    for nm in names:
+        wls.append(Workload(nm, args, torch, dg, stream))
+        log(f"[bench] {nm}: {len(wls[-1].cases)} cases ready "
+            f"({time.perf_counter() - t_gen:.1f} s)")
+
+    steps = args.steps
+    if steps is None:
+        # default: about two seconds of the slowest workload's steps
+        per = max(time_steps(w, torch, stream, 3, None) / 3.0 for w in wls)
+        steps = int(max(20, min(20000, 2000.0 / max(per, 1e-3))))
+        steps = int(max_over_ranks(pg, steps))
+
+    # warm-up, then the timed regions back to back (clocks sampled throughout)
     with torch.cuda.stream(stream):
-        # eager warm-up (device set-up, occupancy queries), then graph capture
-        for _ in range(2):
-            for d in dcs:
-                d.call(stream.cuda_stream)
-        stream.synchronize()
-        if dg.get_device_status(stream.cuda_stream) != 0:
-            raise RuntimeError("device status set during warm-up")
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for d in dcs:
-                d.call(stream.cuda_stream)
-        for _ in range(args.warmup):
-            graph.replay()
-        stream.synchronize()
+        for w in wls:
+            for _ in range(args.warmup):
+                w.graph.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.2)
+    spans = {}
+    for w in wls:
+        a = time.perf_counter()
+        w.ms = time_steps(w, torch, stream, steps, pg)
+        spans[w.name] = (a, time.perf_counter())
+    samples = sampler.stop() if sampler else None
+    status = dg.get_device_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed regions")
 
-        steps = args.steps
-        if steps is None:
-            # default: a timed region of about two seconds
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(5):
-                graph.replay()
-            e1.record(stream)
-            stream.synchronize()
-            per = e0.elapsed_time(e1) / 5.0
-            steps = int(max(20, min(20000, 2000.0 / max(per, 1e-3))))
-            steps = int(max_over_ranks(pg, steps))
-
-        sampler = ClockSampler(local) if rank == 0 else None
-        barrier(pg)
-        torch.cuda.synchronize()
-        if sampler:
-            sampler.start()
-            time.sleep(0.3)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            graph.replay()
-        t1.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-        clocks = sampler.stop() if sampler else None
-        barrier(pg)
-        ms = max_over_ranks(pg, t0.elapsed_time(t1))
-        status = dg.get_device_status(stream.cuda_stream)
-        if status != 0:
-            raise RuntimeError(f"device status {status} after the timed region")
-
-    ms_per_step = ms / steps
-    value = world * step_bytes * steps / (ms / 1e3) / 1e9
-    tflops = world * step_flops * steps / (ms / 1e3) / 1e12
-
-    per_case = per_case_cold(dcs, torch, stream) if (rank == 0 and not args.quick) else None
-    e2e = run_e2e(dcs, cases, torch, stream, min(steps, args.e2e_steps), pg, world)
-    cpu = None
+    detail = {}
+    for w in wls:
+        rec = {"steps": steps, "ms_per_step": round(w.ms / steps, 5), "cases": len(w.cases),
+               "gpu_launches": steps * w.launches}
+        secs = w.ms / 1e3 / steps
+        roof = roofline(w.name, w.cases, secs, peaks, w.launches)
+        rec["unit"] = roof["unit"]
+        rec["value"] = round(value_of(w.cases, secs, roof["unit"]), 1)
+        rec["gbs"] = round(value_of(w.cases, secs, "GB/s"), 1)
+        rec["tflops"] = round(value_of(w.cases, secs, "TFLOP/s"), 1)
+        rec["roofline"] = roof
+        rec["workload"] = w.describe(args)
+        rec["l2"] = w.l2_note()
+        if samples:
+            rec["clocks"] = ClockSampler.summarize(samples, *spans[w.name])
+        detail[w.name] = rec
+    for w in wls:
+        if rank == 0 and not args.quick:
+            detail[w.name]["per_case"] = per_case_cold(w.dcs, torch, stream, peaks)
+        detail[w.name]["e2e"] = run_e2e(w.dcs, w.cases, torch, stream,
+                                        min(steps, args.e2e_steps), pg, world,
+                                        detail[w.name]["unit"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cases)
-
+        import oracle
+        orc = oracle.Oracle()
+        for w in wls:
+            detail[w.name]["cpu_baseline"] = cpu_baseline(
+                orc, w.cases, detail[w.name]["unit"],
+                args.cpu_budget if w.name == head else args.cpu_budget / 2)
     if rank != 0:
         return None
-    hbm, bf16, _bf16_sus, src = measured_peaks()
-    launches_per_step = len(dcs)
-    avg_launch_s = (ms_per_step / 1e3) / launches_per_step
-    if args.workload in HBM_BOUND:
-        achieved = step_bytes / launches_per_step / avg_launch_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": recorded_traffic(args.workload),
-                "peak_source": ("measured HBM copy, MEASURED_PEAKS.json hbm_gbs"
-                                if src == "measured" else "fallback 6.8 TB/s")}
-    else:
-        # dense FP8 tensor peak = bf16 measured x 2 (nominal ratio 4.5 / 2.25 PFLOP/s)
-        fp8_peak = 2.0 * bf16
-        achieved = step_flops / launches_per_step / avg_launch_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "traffic": recorded_traffic(args.workload),
-                "peak_source": (f"{src} bf16 cuBLAS burst x 2 (fp8/bf16 nominal ratio)")}
-    desc = describe(args.workload)
-    if args.add_c:
-        desc += "; D = C + A B with a bf16 addend C read per call"
-    if args.layout != "nt":
-        desc += f"; operands stored as the {args.layout} layout"
-    if args.ue8m0:
-        desc += "; packed UE8M0 scales (the fp32 scales rounded up to powers of two)"
-    if args.case is not None:
-        desc += f" (case {args.case} only: {cases[0].label})"
-    big = footprint > 2 * L2_BYTES
-    return {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+
+    h = detail[head]
+    hw = next(w for w in wls if w.name == head)
+    value = world * h["value"]
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": h["unit"], "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if args.workload == "quantize_act" else "e4m3",
-        "data": data_desc(args.workload),
-        "config": {"workload": desc, "cases": len(cases),
-                   "launch": "one CUDA graph per step (all cases), inputs resident in HBM",
-                   "l2": (f"inputs larger than L2: step footprint {footprint / 1e6:.0f} MB vs "
-                          f"129 MB L2; each case's buffers are evicted by the other cases "
-                          f"before it runs again") if big else
-                         (f"step footprint {footprint / 1e6:.0f} MB: NOT larger than L2, "
-                          f"repeats may hit L2"),
-                   "parallelism": f"replicas x{world}"},
-        "tflops": round(tflops, 1),
-        "roofline": roof,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": steps * launches_per_step,
-        "clocks": clocks,
-        "cases": per_case,
+        "dtype": "f32" if head == "quantize_act" else "e4m3",
+        "data": data_desc(head),
+        "config": {"workload": h["workload"], "cases": h["cases"],
+                   "launch": "one CUDA graph per step (all cases of the workload), inputs "
+                             "resident in HBM",
+                   "l2": h["l2"], "parallelism": f"replicas x{world}",
+                   "other_workloads": [n for n in names if n != head]},
+        "tflops": round(world * h["tflops"], 1), "gbs": round(world * h["gbs"], 1),
+        "roofline": h["roofline"],
+        "cpu_baseline": h.get("cpu_baseline"),
+        "e2e": h["e2e"],
+        "gpu_launches": h["gpu_launches"],
+        "gpu_launches_all_workloads": sum(detail[n]["gpu_launches"] for n in names),
+        "clocks": (ClockSampler.summarize(samples, spans[names[0]][0], spans[names[-1]][1])
+                   if samples else None),
+        "cases": h.get("per_case"),
     }
+    if len(names) > 1:
+        line["per_config"] = detail
+    if hw.footprint <= 2 * L2_BYTES:
+        line["config"]["note"] = "footprint not larger than L2"
+    return line
 
 
-def per_case_cold(dcs, torch, stream, reps=10):
+def per_case_cold(dcs, torch, stream, peaks, reps=10):
     """Per-case kernel time with a cold L2, free of host launch overhead: a
     graph [write a 256 MB buffer, GEMM] and a graph [write the buffer] are each
     replayed `reps` times between CUDA events, and the difference is the
-    GEMM's time.  Runs after the timed region; reported as detail."""
+    GEMM's time.  Runs after the timed regions; reported as detail, each case
+    with the fraction of its own binding roof."""
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     out = []
 
@@ -560,15 +698,19 @@ def per_case_cold(dcs, torch, stream, reps=10):
                 flush.zero_()
                 d.call(stream.cuda_stream)
             us = max(1e-3, min(timed(g1) for _ in range(3)) - t_flush)
-            out.append({"case": d.c.label, "us": round(us, 2),
-                        "gbs": round(d.c.bytes / (us * 1e-6) / 1e9, 1),
-                        "tflops": round(d.c.flops / (us * 1e-6) / 1e12, 1)})
+            c = d.c
+            out.append({"case": c.label, "us": round(us, 2),
+                        "gbs": round(c.bytes / (us * 1e-6) / 1e9, 1),
+                        "tflops": round(c.flops / (us * 1e-6) / 1e12, 1),
+                        "bound": ("hbm" if c.bytes / peaks.hbm / 1e9 >= c.flops / peaks.fp8 / 1e12
+                                  else "tensor"),
+                        "frac_binding": round(peaks.ideal_s(c) / (us * 1e-6), 4)})
             del g1
     del flush
     return out
 
 
-def run_e2e(dcs, cases, torch, stream, steps, pg, world):
+def run_e2e(dcs, cases, torch, stream, steps, pg, world, unit="GB/s"):
     """The same metric through the C ABI, with every step's inputs copied from
     pinned host memory and every output read back to the host."""
     steps = max(3, int(steps))
@@ -609,10 +751,10 @@ def run_e2e(dcs, cases, torch, stream, steps, pg, world):
     for _ in range(steps):
         one_step()
     dt = max_over_ranks(pg, time.perf_counter() - t0)
-    step_bytes = sum(c.bytes for c in cases)
-    return {"value": round(world * step_bytes * steps / dt / 1e9, 1), "unit": "GB/s",
+    per = dt / steps
+    return {"value": round(world * value_of(cases, per, unit), 2), "unit": unit,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
+            "steps": steps, "ms_per_step": round(per * 1e3, 4),
             "copies": "pinned host buffers; inputs on a second stream, overlapping the "
                       "previous case's kernel and result read-back"}
 
@@ -672,32 +814,54 @@ def macs_per_output(c):
     return c.p["K"] / c.p["G"] if c.kind == "k_grouped" else c.p["K"]
 
 
-def cpu_baseline(cases):
+def _sample_shape(c, budget_s, rate, cores):
+    """Rows and columns of a case's oracle sample sized to take about
+    `budget_s` seconds at `rate` output-element MACs per second."""
+    if c.kind == "quantize":
+        return max(1, min(c.m_valid, int(budget_s * rate / c.p["K"]))), 0
+    per_out = macs_per_output(c) * (c.p["G"] if c.kind == "k_grouped" else 1)
+    rows = min(max(cores, c.p["G"]) if c.kind == "masked" else cores, c.m_valid)
+    cols = int(budget_s * rate / (rows * per_out))
+    if cols >= c.p["N"]:
+        # whole rows: as many (a multiple of the core count) as the budget allows
+        rows = int(budget_s * rate / (c.p["N"] * per_out)) // cores * cores
+        rows = max(1, min(c.m_valid, max(rows, cores)))
+    return rows, max(16, min(c.p["N"], cols // 16 * 16))
+
+
+def _calibrate(orc, c, cores):
+    """Output-element MACs (quantiser: elements) per second of the oracle on
+    this host, from a small sample of case c."""
+    s, done, _ = _oracle_sample(orc, c, cores, 128, cores)
+    return done * (1 if c.kind == "quantize" else macs_per_output(c)) / max(s, 1e-6)
+
+
+def cpu_baseline(orc, cases, unit, budget_s):
     """The oracle as it stands, on this host's cores, on a bounded sample of
-    every case: 4 x `cores` whole output rows per case (about 10-20 s on a
-    16-core host for the decode sweep); the time is scaled to the whole case by
-    the ratio of output elements."""
-    import oracle
-    orc = oracle.Oracle()
+    every case of a workload (about `budget_s` seconds in all): each case's
+    sample is sized from a calibration run, and its time scaled to the whole
+    case by the ratio of output elements."""
     cores = len(os.sched_getaffinity(0))
-    rows = 4 * cores
-    t_full, wall, total_bytes = 0.0, 0.0, 0
+    rate = _calibrate(orc, cases[0], cores)
+    t_full, wall, shapes = 0.0, 0.0, []
     for c in cases:
-        secs, done, full = _oracle_sample(orc, c, rows, c.p.get("N", 0), cores)
+        rows, cols = _sample_shape(c, budget_s / len(cases), rate, cores)
+        secs, done, full = _oracle_sample(orc, c, rows, cols, cores)
         wall += secs
         t_full += secs * full / done
-        total_bytes += c.bytes
-    return {"value": round(total_bytes / t_full / 1e9, 4), "unit": "GB/s", "cores": cores,
+        shapes.append(f"{rows}x{cols or c.p['K']}")
+    return {"value": round(value_of(cases, t_full, unit), 5), "unit": unit, "cores": cores,
             "kind": "oracle",
-            "sample": f"{rows} whole output rows per case ({len(cases)} cases; all rows where "
-                      f"a case has fewer); time scaled to the whole case by output elements; "
-                      f"{wall:.1f} s wall",
+            "sample": (f"per case a block of output rows x columns sized for ~{budget_s:.0f} s "
+                       f"in all ({', '.join(shapes)}); time scaled to the whole case by "
+                       f"output elements; {wall:.1f} s wall"),
             "seconds": round(wall, 2)}
 
 
 def run_reference(args):
-    """The CPU oracle timed on this host's cores; step i samples case i mod n,
-    each step sized so the whole run takes about two minutes."""
+    """The CPU oracle timed on this host's cores on the headline workload;
+    step i samples case i mod n, each step sized so the whole run takes about
+    two minutes."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
@@ -705,47 +869,41 @@ def run_reference(args):
     import oracle
     orc = oracle.Oracle()
     cores = len(os.sched_getaffinity(0))
-    cases = make_cases(args.workload, args.case, add_c=args.add_c, layout=args.layout,
+    name = HEADLINE if args.workload == "all" else args.workload
+    cases = make_cases(name, args.case, add_c=args.add_c, layout=args.layout,
                        ue8m0=args.ue8m0)
+    peaks = Peaks()
+    unit = "GB/s" if peaks.bound(cases) == "hbm" else "TFLOP/s"
     steps = args.steps if args.steps is not None else 2 * len(cases)
     warm = args.warmup
     budget = 120.0 / max(1, steps + warm)
-    s, done, _ = _oracle_sample(orc, cases[0], cores, 128, cores)
-    quant = cases[0].kind == "quantize"
-    # output-element MACs (quantiser: elements) per second
-    rate = done * (1 if quant else macs_per_output(cases[0])) / max(s, 1e-6)
-    t_full, bytes_sum, wall = 0.0, 0, 0.0
+    rate = _calibrate(orc, cases[0], cores)
+    t_full, wall = 0.0, 0.0
+    done_cases = []
     for i in range(warm + steps):
         c = cases[i % len(cases)]
-        if quant:
-            rows = max(1, min(c.m_valid, int(budget * rate / c.p["K"])))
-            cols = 0
-        else:
-            rows = min(cores, c.m_valid)
-            per_row = macs_per_output(c) * (c.p["G"] if c.kind == "k_grouped" else 1)
-            cols = int(budget * rate / (rows * per_row))
-            cols = max(16, min(c.p["N"], cols // 16 * 16))
+        rows, cols = _sample_shape(c, budget, rate, cores)
         secs, done, full = _oracle_sample(orc, c, rows, cols, cores)
         if i >= warm:
             wall += secs
             t_full += secs * full / done
-            bytes_sum += c.bytes
-    value = bytes_sum / t_full / 1e9
-    sample = (f"per step one case (round robin over {len(cases)}), {cores} output rows x up to "
-              f"all columns (sized for a ~2 minute run); time scaled to the whole case by "
-              f"output elements")
+            done_cases.append(c)
+    value = value_of(done_cases, t_full, unit)
+    sample = (f"per step one case (round robin over {len(cases)}), a block of output rows x "
+              f"columns sized for a ~2 minute run; time scaled to the whole case by output "
+              f"elements")
     return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": round(wall / steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if args.workload == "quantize_act" else "f64",
-        "data": data_desc(args.workload),
-        "config": {"workload": describe(args.workload), "cases": len(cases),
+        "dtype": "f32" if name == "quantize_act" else "f64",
+        "data": data_desc(name),
+        "config": {"workload": describe(name), "cases": len(cases),
                    "parallelism": "host cores (OpenMP over output rows)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores,
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -755,14 +913,17 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: about two seconds of steps)")
+                    help="timed steps per workload (default: about two seconds of steps)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.CONFIGS), default="dense_decode")
+    ap.add_argument("--workload", choices=["all"] + sorted(W.CONFIGS), default="all")
     ap.add_argument("--case", type=int, default=None,
                     help="run only case I of the workload (profiling one shape)")
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the headline's CPU baseline (half that for "
+                         "each other workload)")
     ap.add_argument("--add-c", action="store_true",
                     help="dense workloads: D = C + A B^T through dg_gemm_fp8_fp8_bf16_nt_add_c "
                          "(a seeded bf16 addend C; its 2*M*N bytes count as read)")
@@ -777,6 +938,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3
+    if args.workload == "all" and (args.add_c or args.layout != "nt" or args.case is not None):
+        ap.error("--add-c, --layout and --case need a single --workload")
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -27,7 +27,17 @@
  *    launched; dg_last_error_string() gives the detail.  Errors found on the
  *    device (a masked_m out of range, a contiguous block that mixes experts, a
  *    bad K-grouped ks entry, an internal wait that timed out) are recorded in a
- *    device status word read by dg_get_device_status().
+ *    device status word read by dg_get_device_status().  There is one such
+ *    word per device, shared by every stream and every call on that device.
+ *  - Bounded waits: every wait inside a kernel (for an operand tile, a tensor-
+ *    memory accumulator, a peer CTA) gives up after a time limit, 2 s unless
+ *    dg_set_wait_timeout_ns() sets another.  A kernel whose wait gives up
+ *    records DG_ERR_TIMEOUT in the status word and finishes WITHOUT its
+ *    result (D is left partly written); the GEMM call itself has already
+ *    returned DG_OK.  A call that can legitimately take longer than the limit
+ *    (a very large problem on a GPU time-sliced with other work) needs a
+ *    larger limit, and callers that must know whether a result is complete
+ *    poll dg_get_device_status().
  *  - The current CUDA device must be a compute capability 10.3 GPU (GB300).
  *
  * Layouts
@@ -259,7 +269,12 @@ const char* dg_last_error_string(void);
 
 /* Waits for `stream`, then returns and clears the device status word of the
  * current device: DG_OK, or the first device-side error recorded since the last
- * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE, DG_ERR_KS_RANGE). */
+ * call (DG_ERR_TIMEOUT, DG_ERR_MASK_RANGE, DG_ERR_EXPERT_RANGE, DG_ERR_KS_RANGE).
+ * The word is per device and shared across streams: an error raised by a
+ * kernel on any stream of the device is reported here, and work still running
+ * on other streams may raise one after this call returns.  The read and the
+ * clear are one atomic exchange on the device (a one-thread kernel on
+ * `stream`), so no error is lost between them. */
 dg_status dg_get_device_status(void* stream);
 
 /* Tile configuration the library would choose (heuristic; no device needed).

@@ -22,7 +22,15 @@
 #include "dg_quant.h"
 
 // The device status word: kernels record the first device-side error here.
+// One word per device, shared by every stream and call on it.
 __device__ unsigned int g_dg_status = 0;
+// Where take_status_kernel leaves the value it took from the status word.
+__device__ unsigned int g_dg_status_taken = 0;
+
+// Reads and clears the status word in one atomic exchange, so that an error
+// raised by a kernel on another stream between the read and the clear is not
+// lost (it stays in the word for the next read).
+__global__ void take_status_kernel() { g_dg_status_taken = atomicExch(&g_dg_status, 0u); }
 
 namespace {
 
@@ -56,6 +64,7 @@ constexpr int kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class GPUs
 constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 8;
 constexpr int kRasterM = 16;
+constexpr int kMaxInstances = 16;    // instances per table (the cluster cache's size)
 
 void read_env_once() {
   int expected = -1;
@@ -261,7 +270,7 @@ struct DeviceState {
   int sms = 0;
   unsigned int* status = nullptr;
   // resident clusters per (instance table, instance, split)
-  int max_clusters[kNumTables][16][kMaxCluster + 1] = {};
+  int max_clusters[kNumTables][kMaxInstances][kMaxCluster + 1] = {};
 };
 
 std::mutex g_mu;
@@ -312,6 +321,9 @@ dg_status device_state(DeviceState** out, int* dev_out) {
   }
   for (int tid = 0; tid < kNumTables; ++tid) {
     const Table tab = table_for(tid);
+    if (tab.n > kMaxInstances)
+      return fail(DG_ERR_CUDA, "instance table %d holds %d instances, more than %d", tid, tab.n,
+                  kMaxInstances);
     for (int i = 0; i < tab.n; ++i)
       if ((e = tab.p[i].set_smem(kMaxSmem)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
@@ -326,6 +338,9 @@ dg_status device_state(DeviceState** out, int* dev_out) {
 int clusters_resident(DeviceState& st, int kind, int inst, const Instance& in, int S, int smem,
                       int num_sms) {
   if (S <= 1) return num_sms;
+  if (inst < 0 || inst >= kMaxInstances || S > kMaxCluster) return 0;
+  // the cache is filled lazily by whichever thread plans first
+  std::lock_guard<std::mutex> lock(g_mu);
   int& slot = st.max_clusters[table_id(kind, in.layout, in.sfp != 0)][inst][S];
   if (slot == 0) {
     int n = 0;
@@ -759,13 +774,15 @@ dg_status dg_get_device_status(void* stream) {
   int dev = 0;
   dg_status s = device_state(&st, &dev);
   if (s != DG_OK) return s;
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned int v = 0, zero = 0;
-  if ((e = cudaMemcpyFromSymbol(&v, g_dg_status, sizeof(v))) != cudaSuccess)
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  take_status_kernel<<<1, 1, 0, cs>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "status read launch");
+  unsigned int v = 0;
+  if ((e = cudaMemcpyFromSymbolAsync(&v, g_dg_status_taken, sizeof(v), 0,
+                                     cudaMemcpyDeviceToHost, cs)) != cudaSuccess)
     return cuda_fail(e, "read status");
-  if ((e = cudaMemcpyToSymbol(g_dg_status, &zero, sizeof(zero))) != cudaSuccess)
-    return cuda_fail(e, "clear status");
+  if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   switch (v) {
     case dgk::ST_OK: return ok();
     case dgk::ST_TIMEOUT: return fail(DG_ERR_TIMEOUT, "a kernel wait timed out");

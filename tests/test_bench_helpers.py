@@ -66,3 +66,46 @@ def test_ue8m0_stand_in_scales():
     assert np.all(sa2[:, :40] >= live) and np.all(sa2[:, :40] < 2 * live)
     assert np.all(sb2 >= p["sb"]) and np.all(sb2 < 2 * p["sb"])
     assert np.all(np.log2(sb2) == np.round(np.log2(sb2)))
+
+
+def _fake(b, bytes_, flops):
+    c = b.Case("dense", dict(A=None, M=64, N=128, K=128), "f")
+    c.bytes, c.flops = bytes_, flops
+    return c
+
+
+def test_binding_roof_fractions():
+    """Each case is judged against the roof it is bound by: its ideal time is
+    the larger of bytes / HBM peak and FLOPs / FP8 peak, and a step's
+    fraction is the sum of the ideal times over the measured time."""
+    b = _bench()
+    pk = b.Peaks()
+    pk.hbm, pk.fp8 = 1000.0, 2000.0          # GB/s, TFLOP/s
+    mem = _fake(b, 1e9, 1e12)                # 1 ms of HBM, 0.5 ms of tensor
+    cmp_ = _fake(b, 1e8, 4e12)               # 0.1 ms of HBM, 2 ms of tensor
+    assert abs(pk.ideal_s(mem) - 1e-3) < 1e-12 and abs(pk.ideal_s(cmp_) - 2e-3) < 1e-12
+    assert pk.bound([mem]) == "hbm" and pk.bound([cmp_]) == "tensor"
+    assert pk.bound([mem, cmp_]) == "tensor"   # 1.1 ms of HBM against 2.5 ms of tensor
+    r = b.roofline("none", [mem, cmp_], 6e-3, pk, 2)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 5e12 / 6e-3 / 1e12) < 0.1
+    assert abs(r["frac"] - (5e12 / 6e-3 / 1e12) / 2000.0) < 1e-4
+    assert abs(r["frac_binding"] - 0.5) < 1e-4            # (1 + 2) ms ideal over 6 ms
+    assert r["cases_hbm_bound"] == 1 and r["cases_tensor_bound"] == 1
+    nom = max(1e9 / 8000e9, 1e12 / 4500e12) + max(1e8 / 8000e9, 4e12 / 4500e12)
+    assert abs(r["frac_binding_nominal"] - nom / 6e-3) < 1e-4
+    assert abs(b.value_of([mem, cmp_], 2.0, "GB/s") - 1.1e9 / 2.0 / 1e9) < 1e-9
+
+
+def test_oracle_sample_shape_fits_the_budget():
+    """A case's oracle sample takes whole rows (a multiple of the core count)
+    once a row block of all columns fits the budget, and never more rows than
+    the case has."""
+    b = _bench()
+    c = b.Case("dense", dict(A=None, M=4096, N=1024, K=1024), "d")
+    rows, cols = b._sample_shape(c, 1.0, 1e9, 8)           # 1e9 MACs: ~950 rows of 1M MACs
+    assert cols == 1024 and rows % 8 == 0 and rows * 1024 * 1024 <= 1e9
+    rows, cols = b._sample_shape(c, 1e-3, 1e9, 8)          # 1e6 MACs: 8 rows x ~120 columns
+    assert rows == 8 and cols % 16 == 0 and cols < 1024
+    rows, cols = b._sample_shape(c, 1e6, 1e9, 8)
+    assert rows == 4096 and cols == 1024

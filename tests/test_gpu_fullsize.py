@@ -2,10 +2,13 @@
 benchmarks), in the configuration the library picks and the bench times.
 
 The GPU computes every output; the oracle recomputes a sample of whole rows
-(first, last and seeded random rows), compared element by element with the
-tolerance.  Properties that hold at any size are checked on every row:
-contiguous padding rows are +0 and masked rows past masked_m keep the sentinel,
-bit for bit, and no output is non-finite."""
+(so every N tile, the last one included, is checked on each sampled row),
+compared element by element with the tolerance: at least one seeded row of
+every 128-row M block (so every raster band, every M block of every expert and
+of every group, and every wave of tiles is touched), plus each M block's first
+and last rows where the oracle cost allows.  Properties that hold at any size
+are checked on every row: contiguous padding rows are +0 and masked rows past
+masked_m keep the sentinel, bit for bit, and no output is non-finite."""
 import numpy as np
 import pytest
 import torch
@@ -35,6 +38,16 @@ def sample_rows(M, k, seed):
     return np.array(sorted(rows), np.int64)
 
 
+def rows_per_block(lo, hi, seed, block=128):
+    """One seeded row in every `block`-row block of [lo, hi), plus lo and
+    hi - 1."""
+    rng = np.random.default_rng(seed)
+    rows = {lo, hi - 1}
+    for b0 in range(lo, hi, block):
+        rows.add(int(rng.integers(b0, min(hi, b0 + block))))
+    return sorted(rows)
+
+
 DECODE = [(m, n, k) for m in (64, 128) for (n, k) in W.DENSE_NK]
 PREFILL = [(4096, n, k) for (n, k) in W.DENSE_NK]
 
@@ -46,7 +59,12 @@ def test_dense_fullsize(shape):
     p = W.dense_problem(M, N, K, seed=seed)
     got = U.run_dense(p)
     assert np.all(np.isfinite(U.bits_to_f64(got)))
-    rows = sample_rows(M, 16 if M <= 128 else 8, seed + N)
+    if M <= 128:
+        rows = sample_rows(M, 16, seed + N)
+    else:
+        # every 128-row M block, hence every raster band of 16 M blocks
+        rows = np.array(rows_per_block(0, M, seed + N), np.int64)
+        assert len(rows) >= M // 128
     want = ORC.gemm_nt_rows(p["A"], p["sa"], p["B"], p["sb"], rows)
     U.assert_close(got[rows], want, f"dense {shape}")
 
@@ -61,13 +79,14 @@ def test_contiguous_fullsize(nk):
     pad = mi < 0
     assert np.all(got[pad] == 0)
     assert np.all(np.isfinite(U.bits_to_f64(got[~pad])))
-    # per expert: its first and last row plus two random rows
-    rng = np.random.default_rng(7)
+    # every 128-row M block of every expert: one seeded row each, plus the
+    # expert's first and last rows
     rows = []
     for e in range(p["G"]):
         r = np.nonzero(mi == e)[0]
-        rows += [r[0], r[-1], *rng.choice(r, 2).tolist()]
+        rows += rows_per_block(int(r[0]), int(r[-1]) + 1, 7 + e)
     rows = np.array(sorted(set(rows)), np.int64)
+    assert len(rows) >= int(np.sum(mi >= 0)) // 128
     want = ORC.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], mi, rows=rows)
     U.assert_close(got[rows], want, f"contiguous {nk}")
 
@@ -84,6 +103,8 @@ def test_masked_fullsize(G, nk):
     for g in range(G):
         v = int(mm[g])
         assert np.all(got[g, v:] == W.BF16_SENTINEL), f"group {g} rows past {v} written"
-        rows = np.array(sorted({0, v - 1, *rng.integers(0, v, size=2).tolist()}), np.int64)
+        # every 128-row M block of the group's valid rows, plus one more random row
+        rows = np.array(sorted({*rows_per_block(0, v, G * 1000 + g),
+                                int(rng.integers(0, v))}), np.int64)
         want = ORC.gemm_nt_rows(p["A"][g], p["sa"][g], p["B"][g], p["sb"][g], rows)
         U.assert_close(got[g][rows], want, f"masked G={G} {nk} group {g}")
