@@ -307,9 +307,11 @@ def value_of(cases, seconds, unit):
 
 # ---------------------------------------------------------------- clocks ---
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons during a region.
+    Each sample carries nvidia-smi's own timestamp, so the samples of a region
+    are found by time even when the tool's output arrives late (buffered)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -333,7 +335,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append((time.perf_counter(), line.strip()))
+            self.lines.append(line.strip())
+
+    def wait_first(self, timeout=3.0):
+        """Block until the first sample has arrived (or `timeout` seconds)."""
+        t = time.time()
+        while self.proc is not None and not self.lines and time.time() - t < timeout:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -350,17 +358,24 @@ class ClockSampler:
     @staticmethod
     def summarize(lines, t0=None, t1=None):
         """Median SM clock, max clock and the throttle reasons seen in the
-        samples taken in [t0, t1] (all samples when not given)."""
+        samples taken in [t0, t1] (wall-clock seconds; all samples when not
+        given)."""
         if not lines:
             return None
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         sm, smax, power, reasons = [], [], [], set()
-        for t, ln in lines:
-            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
-                continue
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and ((t0 is not None and ts < t0) or (t1 is not None and ts > t1)):
+                continue
+            parts = parts[1:]
             try:
                 sm.append(float(parts[0]))
                 smax.append(float(parts[1]))
@@ -594,12 +609,15 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-        time.sleep(0.2)
+        sampler.wait_first()
     spans = {}
     for w in wls:
-        a = time.perf_counter()
+        a = time.time()
         w.ms = time_steps(w, torch, stream, steps, pg)
-        spans[w.name] = (a, time.perf_counter())
+        # (a region shorter than the sampling interval still gets its nearest samples)
+        spans[w.name] = (a - 0.06, time.time() + 0.06)
+    if sampler:
+        time.sleep(0.15)
     samples = sampler.stop() if sampler else None
     status = dg.get_device_status(stream.cuda_stream)
     if status != 0:

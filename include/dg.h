@@ -39,6 +39,14 @@
  *    larger limit, and callers that must know whether a result is complete
  *    poll dg_get_device_status().
  *  - The current CUDA device must be a compute capability 10.3 GPU (GB300).
+ *  - Checked build: the same ABI is also built as libdg_debug.so (every
+ *    kernel compiled with DG_DEBUG=1).  Before each TMA load and each plain
+ *    global store its kernels check the coordinates against the tensors'
+ *    extents, and after each wait on a producer -> consumer ring they check
+ *    that the slot holds the fill they expect.  A failed check skips the
+ *    access, aborts the kernel through the bounded-wait path and records
+ *    DG_ERR_DEBUG_BOUNDS or DG_ERR_DEBUG_PHASE in the status word; nothing
+ *    traps.  It is slower and meant for tests.
  *
  * Layouts
  *  - A  : [M][K] bytes (masked form: [G][max_m][K]).
@@ -71,7 +79,9 @@ typedef enum dg_status {
   DG_ERR_TIMEOUT = 7,           /* device: an internal wait gave up */
   DG_ERR_MASK_RANGE = 8,        /* device: masked_m[g] outside [0, max_m] (clamped) */
   DG_ERR_EXPERT_RANGE = 9,      /* device: m_indices outside [-1, G) or a 128-row block mixes experts */
-  DG_ERR_KS_RANGE = 10          /* device: ks[g] negative, not a multiple of 128, or past K_total */
+  DG_ERR_KS_RANGE = 10,         /* device: ks[g] negative, not a multiple of 128, or past K_total */
+  DG_ERR_DEBUG_BOUNDS = 11,     /* device, checked build only: an access outside a tensor (skipped) */
+  DG_ERR_DEBUG_PHASE = 12       /* device, checked build only: a ring slot held another fill */
 } dg_status;
 
 /* Dense GEMM (DeepGEMM "gemm_fp8_fp8_bf16_nt", deepep.org/zh/deepgemm, "接口设计").
@@ -328,6 +338,17 @@ dg_status dg_debug_force_config(int block_n, int split_k);
  * have no pair kernel, so 1 makes them return DG_ERR_UNSUPPORTED_SHAPE).  The
  * environment variable DG_FORCE_PAIR=0|1 sets the same before the first call. */
 dg_status dg_debug_force_pair(int mode);
+
+/* Test and benchmark hook for the packed-UE8M0 entry points: -1 (default)
+ * lets the heuristic choose between the block-scaled kernels (the tensor
+ * cores apply the UE8M0 scales, tcgen05.mma kind::mxf8f6f4 with block
+ * scaling, and accumulate all of a tile's K in tensor memory) and the
+ * kernels that decode the scales into the per-K-group promotion (which also
+ * hold the K-split forms); 0 never the block-scaled ones, 1 only those (a
+ * shape or forced configuration without one returns DG_ERR_UNSUPPORTED_SHAPE).
+ * Results agree within the stated tolerance either way.  The environment
+ * variable DG_FORCE_BLOCK_SCALED=0|1 sets the same before the first call. */
+dg_status dg_debug_force_block_scaled(int mode);
 
 #ifdef __cplusplus
 }

@@ -23,16 +23,21 @@ __all__ = [
     "m_grouped_gemm_fp8_fp8_bf16_nt_masked", "quantize_fp8_1x128", "get_num_sms", "set_num_sms",
     "get_tma_aligned_size", "get_mk_alignment_for_contiguous_layout", "get_device_status",
     "plan_config", "num_output_tiles", "set_wait_timeout_ns", "debug_set_skip_producer",
-    "debug_force_config", "debug_force_pair", "STATUS_NAMES", "EXPORTED_SYMBOLS",
+    "debug_force_config", "debug_force_pair", "debug_force_block_scaled", "STATUS_NAMES",
+    "EXPORTED_SYMBOLS",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdg.so")
+#: the checked build (bounds and ring-fill checks in every kernel), loaded in
+#: place of libdg.so when the environment sets DG_DEBUG=1
+LIB_DEBUG_PATH = os.path.join(HERE, "libdg_debug.so")
 
 STATUS_NAMES = {
     0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED_SHAPE", 3: "DG_ERR_MISALIGNED",
     4: "DG_ERR_NO_DEVICE", 5: "DG_ERR_ARCH", 6: "DG_ERR_CUDA", 7: "DG_ERR_TIMEOUT",
     8: "DG_ERR_MASK_RANGE", 9: "DG_ERR_EXPERT_RANGE", 10: "DG_ERR_KS_RANGE",
+    11: "DG_ERR_DEBUG_BOUNDS", 12: "DG_ERR_DEBUG_PHASE",
 }
 
 #: Every function include/dg.h declares.
@@ -50,7 +55,7 @@ EXPORTED_SYMBOLS = [
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_num_output_tiles",
     "dg_set_wait_timeout_ns", "dg_debug_set_skip_producer", "dg_debug_force_config",
-    "dg_debug_force_pair",
+    "dg_debug_force_pair", "dg_debug_force_block_scaled",
 ]
 
 
@@ -76,10 +81,11 @@ def lib():
     """The loaded library.  Raises if it has not been built (no fallback)."""
     global _LIB
     if _LIB is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+        path = LIB_DEBUG_PATH if os.environ.get("DG_DEBUG", "0") not in ("", "0") else LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
                                "`python -m moe_grouped_gemm_bf16_gb300._build`")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         L.dg_gemm_fp8_fp8_bf16_nt.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]
         L.dg_gemm_fp8_fp8_bf16_nt_add_c.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                                     _vp]
@@ -118,6 +124,7 @@ def lib():
         L.dg_debug_set_skip_producer.argtypes = [_i]
         L.dg_debug_force_config.argtypes = [_i, _i]
         L.dg_debug_force_pair.argtypes = [_i]
+        L.dg_debug_force_block_scaled.argtypes = [_i]
         for f in EXPORTED_SYMBOLS:
             if f not in ("dg_last_error_string", "dg_num_output_tiles"):
                 getattr(L, f).restype = _i
@@ -309,3 +316,8 @@ def debug_force_config(block_n=0, split_k=0):
 
 def debug_force_pair(mode=-1):
     _check(lib().dg_debug_force_pair(int(mode)))
+
+
+def debug_force_block_scaled(mode=-1):
+    """-1 heuristic, 0 never, 1 only the block-scaled kernels (packed UE8M0 forms)."""
+    _check(lib().dg_debug_force_block_scaled(int(mode)))

@@ -16,8 +16,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdg.so")
+LIB_DEBUG = os.path.join(HERE, "libdg_debug.so")
 
-SOURCES = ["dg_host.cu", "dg_inst_dense.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_mn.cu", "dg_inst_ue8m0.cu", "dg_inst_ue8m0_mn.cu", "dg_quant.cu"]
+SOURCES = ["dg_host.cu", "dg_inst_dense.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_mn.cu", "dg_inst_ue8m0.cu", "dg_inst_ue8m0_mn.cu", "dg_inst_bs.cu",
+           "dg_inst_bs_mn.cu", "dg_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,18 +35,26 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force=False, verbose=False):
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, debug=False):
+    """Compile the library.  debug=True builds the checked library
+    libdg_debug.so instead (every kernel compiled with -DDG_DEBUG=1: bounds
+    checks before each TMA load and plain global store, fill checks after
+    each ring wait, failures reported in the device status word)."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps():
+        return lib
+    bdir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     flags = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-I", INCLUDE,
              "-I", CSRC]
+    if debug:
+        flags += ["-DDG_DEBUG=1"]
     if verbose:
         flags += ["-Xptxas", "-v"]
 
     def one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -56,15 +66,15 @@ def build(force=False, verbose=False):
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", *ARCH, "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    print(build(force=True, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

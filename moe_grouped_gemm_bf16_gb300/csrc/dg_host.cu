@@ -16,6 +16,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "dg.h"
 #include "dg_instances.cuh"
@@ -59,18 +60,22 @@ std::atomic<int> g_skip_producer{0};
 std::atomic<int> g_force_bn{-1};     // -1: not read from the environment yet; 0: auto
 std::atomic<int> g_force_split{0};
 std::atomic<int> g_force_pair{-1};   // -1: heuristic; 0: no pair form; 1: pair form only
+std::atomic<int> g_force_bs{-1};     // -1: heuristic; 0: no block-scaled kernel; 1: only those
 
 constexpr int kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class GPUs
 constexpr int kMaxDevices = 64;
 constexpr int kMaxCluster = 8;
 constexpr int kRasterM = 16;
-constexpr int kMaxInstances = 16;    // instances per table (the cluster cache's size)
+constexpr int kMaxInstances = 32;    // instances per table (the cluster cache's size)
 
 void read_env_once() {
   int expected = -1;
   if (!g_force_bn.compare_exchange_strong(expected, 0)) return;
   // DG_FORCE_PAIR=0|1 (tests and benchmarks only): as dg_debug_force_pair
   if (const char* s = std::getenv("DG_FORCE_PAIR")) g_force_pair.store(std::atoi(s) ? 1 : 0);
+  // DG_FORCE_BLOCK_SCALED=0|1 (tests and benchmarks only): as dg_debug_force_block_scaled
+  if (const char* s = std::getenv("DG_FORCE_BLOCK_SCALED"))
+    g_force_bs.store(std::atoi(s) ? 1 : 0);
   // DG_FORCE_CONFIG="block_n,split_k" (tests and benchmarks only)
   if (const char* s = std::getenv("DG_FORCE_CONFIG")) {
     int bn = 0, sp = 0;
@@ -94,8 +99,24 @@ struct Table {
 
 // Instance tables: 0 dense nt, 1 contiguous, 2 masked, 3 MN-major operands
 // (dense nn / tn / tt and the K-grouped form); 4-7 the same with packed UE8M0
-// scales.
+// scales: the block-scaled instances first, then those that decode the scales
+// into the promotion (which also hold the K-split forms).
 constexpr int kNumTables = 8;
+
+// Block-scaled and promotion instances of one packed-UE8M0 table, concatenated
+// once (thread-safe static initialisation).
+template <const dgk::Instance* (*BS)(int*), const dgk::Instance* (*SFP)(int*)>
+Table joined() {
+  static const std::vector<Instance> all = [] {
+    int nb = 0, ns = 0;
+    const Instance* b = BS(&nb);
+    const Instance* f = SFP(&ns);
+    std::vector<Instance> v(b, b + nb);
+    v.insert(v.end(), f, f + ns);
+    return v;
+  }();
+  return Table{all.data(), static_cast<int>(all.size())};
+}
 
 int table_id(int kind, int layout, bool sfp = false) {
   return ((layout != dgk::kNT || kind == dgk::kKGrouped) ? 3 : kind) + (sfp ? 4 : 0);
@@ -108,16 +129,18 @@ Table table_for(int tid) {
     case 1: t.p = dgk::instances_contiguous(&t.n); break;
     case 2: t.p = dgk::instances_masked(&t.n); break;
     case 3: t.p = dgk::instances_mn(&t.n); break;
-    case 4: t.p = dgk::instances_dense_ue8m0(&t.n); break;
-    case 5: t.p = dgk::instances_contiguous_ue8m0(&t.n); break;
-    case 6: t.p = dgk::instances_masked_ue8m0(&t.n); break;
-    default: t.p = dgk::instances_mn_ue8m0(&t.n); break;
+    case 4: t = joined<dgk::instances_bs_dense, dgk::instances_dense_ue8m0>(); break;
+    case 5: t = joined<dgk::instances_bs_contiguous, dgk::instances_contiguous_ue8m0>(); break;
+    case 6: t = joined<dgk::instances_bs_masked, dgk::instances_masked_ue8m0>(); break;
+    default: t = joined<dgk::instances_bs_mn, dgk::instances_mn_ue8m0>(); break;
   }
   return t;
 }
 
 int smem_for(const Instance& in, int kb, int num_groups) {
-  int s = in.fixed_smem + 3 * kb * 4 +
+  // the promotion kernels keep a tile's B scales in shared memory; the
+  // block-scaled ones read them into the scale-factor staging instead
+  int s = in.fixed_smem + (in.bs ? 0 : 3 * kb * 4) +
           (in.mode == dgk::kMasked     ? (2 * num_groups + 1) * 4
            : in.mode == dgk::kKGrouped ? (num_groups + 1) * 4
                                        : 0);
@@ -154,10 +177,15 @@ struct Plan {
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
   (void)kind; (void)n; (void)num_groups;
-  const double t_cad = in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
+  // block-scaled: the MMA alone (2 cycles per column per K group at ~1.9 GHz)
+  const double t_cad = in.bs ? in.block_n * 2.0 / 1900.0
+                             : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
   const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
-  const double head = 3.06, tail = S > 1 ? 4.9 : 1.6, per_tile = 0.92, fixed = 1.9;
+  // a block-scaled kernel with one accumulator waits for each tile's epilogue
+  // to read it before the next tile's MMAs
+  const double head = 3.06, tail = S > 1 ? 4.9 : 1.6, fixed = 1.9;
+  const double per_tile = 0.92 + (in.bs && in.nacc == 1 ? 0.4 : 0.0);
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
   // the A box the TMA fills per K group (rows past M are zero-filled, not free)
@@ -215,9 +243,13 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     // The CTA-pair form measured slower than the 128-row form on every shape
     // so far (its promotion, not the MMA, sets the pace): it runs only when
     // forced.
+    // (the block-scaled pair form is the heuristic's own choice)
     const int fp = g_force_pair.load();
-    if (fp <= 0 && in.pair) continue;
+    if (fp == 0 && in.pair) continue;
+    if (fp < 0 && in.pair && !in.bs) continue;
     if (fp == 1 && !in.pair) continue;
+    const int fbs = g_force_bs.load();
+    if ((fbs == 0 && in.bs) || (fbs == 1 && !in.bs)) continue;
     if (forced && in.a_rows == 128 && in.split && m_rows <= 64 && has_split64(tab)) continue;
     const int smem = smem_for(in, kb, num_groups);
     if (smem > kMaxSmem) continue;
@@ -527,10 +559,12 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
 
   dgk::Maps maps;
   const bool has_c = kind == dgk::kDense || kind == dgk::kKGrouped;
+  // rows of B per TMA box: the tile, half of it per CTA of a pair, or (block-
+  // scaled pair) 64 rows, two boxes per 128-column block
+  const int b_box = in.pair ? (in.bs ? 64 : in.block_n / 2) : in.block_n;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
-                (kind == dgk::kDense || kind == dgk::kKGrouped) ? 1 : G,
-                in.pair ? in.block_n / 2 : in.block_n, in.a_rows, has_c ? C : nullptr, layout,
-                kind == dgk::kKGrouped ? G : 0, sf_packed);
+                (kind == dgk::kDense || kind == dgk::kKGrouped) ? 1 : G, b_box, in.a_rows,
+                has_c ? C : nullptr, layout, kind == dgk::kKGrouped ? G : 0, sf_packed);
   if (s != DG_OK) return s;
 
   dgk::Params p{};
@@ -547,6 +581,8 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   p.split_k = pl.split;
   p.sb = sb;
   p.kbp = (K / 128 + 3) / 4;
+  p.sa_packed = sf_packed ? static_cast<const void*>(sa) : nullptr;
+  p.ld_sa = ld_sa;
   p.m_indices = kind == dgk::kContiguous ? idx : nullptr;
   p.masked_m = kind == dgk::kMasked ? idx : nullptr;
   p.D = static_cast<uint16_t*>(D);
@@ -563,10 +599,11 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
   }
   if (print_configs())
     std::fprintf(stderr,
-                 "[dg] %s %s M=%d N=%d K=%d G=%d: block_n=%d split_k=%d stages=%d tiles=%lld "
-                 "grid=%d smem=%d\n",
-                 kind_name(kind), layout_name(layout), rows, N, K, G, in.block_n, pl.split, in.stages,
-                 (long long)pl.tiles, grid, pl.smem);
+                 "[dg] %s %s%s M=%d N=%d K=%d G=%d: block_n=%d split_k=%d pair=%d stages=%d "
+                 "tiles=%lld grid=%d smem=%d%s\n",
+                 kind_name(kind), layout_name(layout), sf_packed ? " ue8m0" : "", rows, N, K, G,
+                 in.block_n, pl.split, in.pair, in.stages, (long long)pl.tiles, grid, pl.smem,
+                 in.bs ? " block-scaled" : "");
   return ok();
 }
 
@@ -791,6 +828,10 @@ dg_status dg_get_device_status(void* stream) {
       return fail(DG_ERR_EXPERT_RANGE, "m_indices out of range or a block mixes experts");
     case dgk::ST_KS_RANGE:
       return fail(DG_ERR_KS_RANGE, "ks: a negative or partial K group, or past K_total");
+    case dgk::ST_DEBUG_BOUNDS:
+      return fail(DG_ERR_DEBUG_BOUNDS, "checked build: an access outside a tensor was skipped");
+    case dgk::ST_DEBUG_PHASE:
+      return fail(DG_ERR_DEBUG_PHASE, "checked build: a ring slot held another fill");
     default: return fail(DG_ERR_CUDA, "unknown device status %u", v);
   }
 }
@@ -854,6 +895,13 @@ dg_status dg_debug_set_skip_producer(int on) {
 dg_status dg_debug_force_pair(int mode) {
   if (mode < -1 || mode > 1) return fail(DG_ERR_INVALID_ARG, "pair mode %d", mode);
   g_force_pair.store(mode);
+  return ok();
+}
+
+dg_status dg_debug_force_block_scaled(int mode) {
+  if (mode < -1 || mode > 1) return fail(DG_ERR_INVALID_ARG, "block-scaled mode %d", mode);
+  read_env_once();
+  g_force_bs.store(mode);
   return ok();
 }
 

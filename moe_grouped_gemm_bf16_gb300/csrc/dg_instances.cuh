@@ -22,6 +22,8 @@ struct Instance {
   int pair;        // 1: CTA-pair form (cta_group::2, 256-row tiles over a 2-CTA cluster)
   int layout;      // operand storage (kNT, kNN, kTN, kTT)
   int sfp;         // 1: packed UE8M0 scales
+  int bs;          // 1: block-scaled MMA (the tensor cores apply the UE8M0 scales; no promotion)
+  int nacc;        // block-scaled: tensor-memory accumulators (tiles in flight)
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
                         cudaStream_t s);
@@ -40,6 +42,11 @@ const Instance* instances_dense_ue8m0(int* count);
 const Instance* instances_contiguous_ue8m0(int* count);
 const Instance* instances_masked_ue8m0(int* count);
 const Instance* instances_mn_ue8m0(int* count);
+// block-scaled instances for packed UE8M0 scales (defined in dg_inst_bs*.cu)
+const Instance* instances_bs_dense(int* count);
+const Instance* instances_bs_contiguous(int* count);
+const Instance* instances_bs_masked(int* count);
+const Instance* instances_bs_mn(int* count);
 
 }  // namespace dgk
 
@@ -101,8 +108,71 @@ struct InstanceOf {
 
   static Instance make() {
     return Instance{BN, STAGES, SPLIT ? 1 : 0, MODE, AROWS, PAIR ? 1 : 0, LAYOUT, SFP ? 1 : 0,
-                    SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF + 1024, &launch,
+                    0, 0, SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF + 1024, &launch,
                     &set_smem, &max_clusters};
+  }
+};
+
+}  // namespace dgk
+#endif
+
+#ifdef DGK_DEFINE_BS_INSTANCES
+#include "dg_kernel_bs.cuh"
+
+namespace dgk {
+
+// A block-scaled instance: the same launch interface as InstanceOf.
+template <int BN, int STAGES, int MODE, bool PAIR, int NACC, int LAYOUT = kNT>
+struct BsInstanceOf {
+  static constexpr auto kernel = fp8_gemm_bs_kernel<BN, STAGES, MODE, PAIR, NACC, LAYOUT>;
+
+  static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
+                            cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (PAIR) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = cluster;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.sa, m.d, m.c, p);
+  }
+
+  static cudaError_t set_smem(int smem) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  }
+
+  static cudaError_t max_clusters(int cluster, int smem, int* out) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
+  }
+
+  static Instance make() {
+    return Instance{BN, STAGES, 0, MODE, BLOCK_M, PAIR ? 1 : 0, LAYOUT, 1, 1, NACC,
+                    BsLayout<BN, STAGES, PAIR, NACC>::DYN_OFF + 1024, &launch, &set_smem,
+                    &max_clusters};
   }
 };
 

@@ -73,7 +73,10 @@ struct SmemLayout {
                        T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
                        MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, NUM_BARS = C_FULL + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
-  static constexpr int DYN_OFF = MISC_OFF + 16;            // sb tile, then masked tables
+  // checked build: fill counters of the operand ring's and the scale ring's slots
+  static constexpr int DBG_OFF = MISC_OFF + 16;
+  static constexpr int DBG_BYTES = kDebug ? ((STAGES + SA_SLOTS) * 4 + 15) / 16 * 16 : 0;
+  static constexpr int DYN_OFF = DBG_OFF + DBG_BYTES;      // sb tile, then masked tables
   static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   // TMEM accumulators (K groups the MMA may run ahead of the promotion warps):
@@ -116,6 +119,14 @@ __device__ __forceinline__ float ue8m0_scale(uint32_t word, int g) {
 
 __device__ __forceinline__ void raise_status(const Params& p, unsigned int code) {
   atomicCAS(p.status, 0u, code);
+}
+
+// Checked build: record a failed check and abort the CTA (every later wait
+// returns at once and no further TMA or MMA is issued).
+__device__ __forceinline__ void dbg_fail(const Params& p, unsigned int code,
+                                         volatile uint32_t* abort_flag) {
+  raise_status(p, code);
+  *abort_flag = 1;
 }
 
 // Tile t of the persistent schedule.  Tiles are numbered in raster bands of
@@ -196,6 +207,18 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
   }
   T.zd = T.z;
   return T;
+}
+
+// Checked build: the coordinates of a tile's loads for K group g lie inside
+// the tensors (a pair's second half may start past M: its rows are zero-filled
+// by design).
+template <int MODE, bool PAIR>
+__device__ __forceinline__ bool dbg_tile_ok(const Params& p, const Tile& T, int g) {
+  const int zmax = MODE == kMasked ? p.num_groups : 1;
+  const int emax = (MODE == kContiguous || MODE == kMasked) ? p.num_groups : 1;
+  return g >= T.kbeg && g < T.kend && T.kbeg >= 0 && T.kend <= p.kb && T.m0 >= 0 &&
+         T.m0 < p.M + (PAIR ? BLOCK_M : 0) && T.n0 >= 0 && T.n0 < p.N && T.z >= 0 && T.z < zmax &&
+         T.e >= 0 && T.e < emax && T.zd >= 0 && T.zd < p.num_groups;
 }
 
 __device__ __forceinline__ int num_tiles_dense(const Params& p) {
@@ -290,6 +313,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   int* prefix = reinterpret_cast<int*>(sb_s + 3 * p.kb);
   int* mcnt = prefix + p.num_groups + 1;
   const float* sa_ring = reinterpret_cast<const float*>(smem + L::SA_OFF);
+  // checked build: fills of each operand-ring slot, then of each scale-ring slot
+  volatile uint32_t* dbg_fill = reinterpret_cast<volatile uint32_t*>(smem + L::DBG_OFF);
+  volatile uint32_t* dbg_sa_fill = dbg_fill + STAGES;
 
   const uint32_t crank = (SPLIT || PAIR) ? cluster_ctarank() : 0;
   const int S = SPLIT ? p.split_k : 1;           // CTAs sharing one tile's K groups
@@ -323,6 +349,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
     mbar_init(bar(L::C_FULL), 1);
     misc[1] = 0;
+    if constexpr (kDebug)
+      for (int i = 0; i < STAGES + SA_SLOTS; ++i) dbg_fill[i] = 0;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -440,7 +468,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
         if (T.skip) continue;
         for (int g = T.kbeg; g < T.kend; ++g) {
-          if (wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p)) {
+          bool go = wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p);
+          if constexpr (kDebug) {
+            if (go && !dbg_tile_ok<MODE, PAIR>(p, T, g)) {
+              dbg_fail(p, ST_DEBUG_BOUNDS, abort_flag);
+              go = false;
+            }
+            if (go) dbg_fill[s] = dbg_fill[s] + 1;
+          }
+          if (go) {
             if constexpr (PAIR) {
               // both CTAs' loads complete on the leader's FULL barrier, which
               // expects the bytes of both
@@ -485,7 +521,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // the scales of this and the next SA_GROUPS-1 K groups (groups past
           // the tensor's end read as zero and are not used)
           if ((g - T.kbeg) % SA_GROUPS == 0) {
-            if (wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p)) {
+            bool sgo = wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p);
+            if constexpr (kDebug) {
+              if (sgo && (g < 0 || (SFP ? (g >> 2) >= p.kbp : g >= p.kb))) {
+                dbg_fail(p, ST_DEBUG_BOUNDS, abort_flag);
+                sgo = false;
+              }
+              if (sgo) dbg_sa_fill[j] = dbg_sa_fill[j] + 1;
+            }
+            if (sgo) {
               if constexpr (SFP) {
                 mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_PACKED_BYTES);
                 tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j), T.m0,
@@ -538,10 +582,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int me = warp - 1;
       int s = 0, b = 0, turn = 0;
       uint32_t ph = 0, bph = 0;
+      uint32_t q = 0;   // K groups of this CTA's sequence so far (both issuers' turns)
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
         const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
         if (T.skip) continue;
-        for (int g = T.kbeg; g < T.kend; ++g) {
+        for (int g = T.kbeg; g < T.kend; ++g, ++q) {
           const bool mine = (turn == me);
           if (++turn == NUM_ISSUERS) turn = 0;
           if (!mine) {
@@ -551,8 +596,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
           const bool ok_t = wait_bar(bar(L::T_EMPTY + b), bph ^ 1, abort_flag, p);
           tc_fence_after();
-          const bool ok_f = wait_bar(bar(L::FULL + s), ph, abort_flag, p);
+          bool ok_f = wait_bar(bar(L::FULL + s), ph, abort_flag, p);
           tc_fence_after();
+          if constexpr (kDebug) {
+            // the stage holds this group's fill: its (q / STAGES + 1)-th
+            if (ok_f && dbg_fill[s] != q / STAGES + 1) {
+              dbg_fail(p, ST_DEBUG_PHASE, abort_flag);
+              ok_f = false;
+            }
+          }
           if (ok_t && ok_f) {
             const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
             const uint32_t a_src = sbase + L::A_OFF + s * L::A_BYTES;
@@ -599,6 +651,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t out_s = sbase + L::OUT_OFF;
     int b = 0, j = 0;
     uint32_t bph = 0, jph = 0;
+    uint32_t jn = 0;                    // scale-ring slots consumed (checked build)
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
     uint32_t cph = 0;                   // phase of the addend's barrier
     float acc[HALF];
@@ -658,7 +711,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           };
           const int r = (g - T.kbeg) % SA_GROUPS;   // place in the scale slot
           wait_bar(bar(L::T_FULL + b), bph, abort_flag, p);
-          if (r == 0) wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
+          if (r == 0) {
+            const bool ok_sa = wait_bar(bar(L::SA_FULL + j), jph, abort_flag, p);
+            if constexpr (kDebug) {
+              if (ok_sa && dbg_sa_fill[j] != jn / SA_SLOTS + 1) dbg_fail(p, ST_DEBUG_PHASE, abort_flag);
+            }
+          }
           __syncwarp();
           tc_fence_after();
           // warps whose TMEM lanes hold no loaded row of A have nothing to add
@@ -709,6 +767,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::SA_EMPTY + j));
             if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+            ++jn;
           }
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
           if (load_c && g == g_c) issue_c();
@@ -787,6 +846,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               const uint32_t src = out_s + (cu >> 2) * (BLOCK_M * 64) + r * 64 +
                                    (((cu & 3) ^ ((r >> 1) & 3)) << 4);
               const uint4 w = ld_shared_v4(src);
+              if constexpr (kDebug) {
+                if (T.z >= p.num_groups || T.m0 + r >= p.M || n + 8 > p.N) {
+                  raise_status(p, ST_DEBUG_BOUNDS);
+                  continue;
+                }
+              }
               *reinterpret_cast<uint4*>(
                   p.D + (static_cast<size_t>(T.z) * p.M + T.m0 + r) * p.N + n) = w;
             }
@@ -890,6 +955,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             sum.w += __uint_as_float(cpre[it].y & 0xFFFF0000u);
           }
           const int n = T.n0 + cu * 4;
+          if constexpr (kDebug) {
+            if (n < p.N && T.m0 + grow >= p.M) {
+              raise_status(p, ST_DEBUG_BOUNDS);
+              continue;
+            }
+          }
           if (n < p.N && !*abort_flag) {
             uint2 w;
             w.x = pack_bf16x2(sum.x, sum.y);

@@ -46,12 +46,26 @@ constexpr int MAX_GROUPS_KGROUPED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
 constexpr int MAX_SPLIT = 8;  // CTAs per cluster in the K-split form
 
+// Checked build (compiled with -DDG_DEBUG=1; the library libdg_debug.so):
+// before every TMA load and every plain global store the kernels check the
+// coordinates against the tensors' extents, and after every wait on a
+// producer -> consumer ring barrier the consumer checks that the slot holds
+// the fill it expects (a wait that passed a phase early would see another).
+// A failed check records ST_DEBUG_BOUNDS / ST_DEBUG_PHASE in the status word,
+// skips the access and aborts the CTA (the bounded-wait path); nothing traps.
+#ifndef DG_DEBUG
+#define DG_DEBUG 0
+#endif
+constexpr bool kDebug = DG_DEBUG != 0;
+
 // Device status word values (first error wins).
 constexpr unsigned int ST_OK = 0;
 constexpr unsigned int ST_TIMEOUT = 7;      // an mbarrier wait gave up
 constexpr unsigned int ST_MASK_RANGE = 8;   // masked_m[g] outside [0, max_m]; clamped
 constexpr unsigned int ST_EXPERT_RANGE = 9; // m_indices out of range or a block mixes experts
 constexpr unsigned int ST_KS_RANGE = 10;    // ks[g] negative, not a multiple of 128, or past K
+constexpr unsigned int ST_DEBUG_BOUNDS = 11; // checked build: an access outside a tensor, skipped
+constexpr unsigned int ST_DEBUG_PHASE = 12;  // checked build: a ring slot held another fill
 
 // Debug flags (tests of the failure path only).
 constexpr unsigned int DBG_SKIP_PRODUCER = 1u;  // the TMA warp issues nothing
@@ -70,6 +84,9 @@ struct Params {
   const float* sb;             // [G][nb][kb] fp32, or [G][nb][kbp] packed UE8M0 words (the
                                // instance's SFP parameter says which)
   int kbp;                     // ceil(kb / 4): packed words per row of scales
+  const void* sa_packed;       // packed UE8M0 activation scales [z][kbp][ld_sa] (block-scaled
+                               // kernels read them directly), else null
+  int ld_sa;                   // leading dimension of the activation scales
   const int32_t* m_indices;    // contiguous: [M_total]
   const int32_t* masked_m;     // masked: [G]
   const int32_t* ks;           // K-grouped: [G] K rows of each group (multiples of 128)

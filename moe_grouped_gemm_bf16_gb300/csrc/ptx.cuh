@@ -37,6 +37,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
+// cluster, with release semantics at cluster scope (the arriving thread's
+// earlier writes are visible to a peer that acquires the barrier's phase).
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+               : "memory");
+}
+
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
 // cluster, relaxed: a pure signal that publishes no memory writes.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar, uint32_t rank) {
   uint32_t remote;
@@ -196,6 +206,57 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// ---- Block-scaled MMA (kind::mxf8f6f4.block_scale): the tensor core applies
+// one UE8M0 scale per row of A and per row (column of the output) of B to each
+// 32-deep slice of K, and accumulates in fp32.  The scale factors live in
+// tensor memory at [sfa] and [sfb]; the instruction descriptor's scale-factor
+// ids pick the byte of each 32-bit tensor-memory cell that applies.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8f6f4_bs_pair(uint32_t d_tmem, uint64_t adesc,
+                                                     uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> tensor memory copies (asynchronous, in issue order with the
+// same thread's later MMAs).  128x128b: 128 rows of 16 bytes into lanes
+// taddr.lane .. +127, 4 columns each; 32x128b.warpx4: 32 rows of 16 bytes
+// into the 32 lanes of every lane quarter (the same data four times).
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Pair forms: issued by the leader, each CTA of the pair copies from its own
+// shared memory into its own tensor memory at the same addresses.
+__device__ __forceinline__ void tmem_cp_128x128b_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // ---- CTA-pair (cta_group::2) forms: the two CTAs of a cluster pair share one
 // MMA of M = 256 (each CTA holds 128 rows of A, half of B and its own 128
 // accumulator lanes).  Allocation, deallocation and the relinquish are done
@@ -282,6 +343,31 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mnmajor(uint32_t smem_addr, 
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Shared-memory descriptor of a plain (unswizzled) matrix of 16-byte rows:
+// core matrices of 8 rows x 16 bytes (128 contiguous bytes), `sbo` bytes
+// apart along the rows (128: the rows are simply consecutive).  The source of
+// the tensor-memory copies.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t smem_addr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;  // leading byte offset (one core matrix along K: unused)
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;                              // bits 61-63 = 0: no swizzle
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale-factor
+// id at bits 4-5, A and B e4m3 (bits 7-9, 10-12 = 0), transpose bits 15 / 16
+// for MN-major operands, N >> 3 at bits 17-22, scale type UE8M0 (bit 23 = 1),
+// M >> 4 at bits 24-28, A scale-factor id at bits 29-30.  The ids select the
+// byte of the 32-bit tensor-memory cell that holds the scale.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int m, int n, bool a_mn, bool b_mn,
+                                                      uint32_t sfa_id, uint32_t sfb_id) {
+  return ((sfb_id & 3u) << 4) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) | ((sfa_id & 3u) << 29);
 }
 
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B e4m3

@@ -284,3 +284,13 @@ def test_force_config_hook(L):
     finally:
         dg.debug_force_config(0, 0)
         dg.debug_force_pair(-1)
+
+
+def test_checked_build_exports_every_declared_symbol():
+    """The checked library (every kernel compiled with DG_DEBUG=1) builds on
+    a machine without a GPU and exports the same ABI."""
+    path = _build.build(debug=True)
+    assert os.path.basename(path) == "libdg_debug.so"
+    Ld = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(Ld, name), name

@@ -1,6 +1,9 @@
-"""Packed UE8M0 scales through the C ABI against the CPU oracle: the dense,
-contiguous and masked GEMMs (every dense instance forced, K splits whose
-slices start inside a packed word), and the UE8M0 quantiser bit for bit."""
+"""Packed UE8M0 scales through the C ABI against the CPU oracle, on the kernels
+that decode the scales into the per-K-group promotion (the block-scaled
+kernels, which the heuristic prefers for these entry points, are switched off
+here and tested in their own module): the dense, contiguous and masked GEMMs
+(every dense instance forced, K splits whose slices start inside a packed
+word), and the UE8M0 quantiser bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -22,6 +25,9 @@ def built():
     _build.build()
     ORC = oracle.Oracle()
     torch.cuda.init()
+    dg.debug_force_block_scaled(0)
+    yield
+    dg.debug_force_block_scaled(-1)
 
 
 def _exponents(shape, seed, lo=118, hi=136):
