@@ -177,8 +177,10 @@ struct Plan {
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
   (void)kind; (void)n; (void)num_groups;
-  // block-scaled: the MMA alone (2 cycles per column per K group at ~1.9 GHz)
-  const double t_cad = in.bs ? in.block_n * 2.0 / 1900.0
+  // block-scaled: the slower of the MMA (2 cycles per column per K group at
+  // ~1.9 GHz) and the issuing thread's loop per K group (~620 cycles with
+  // one issuer, measured; two issuers share it)
+  const double t_cad = in.bs ? std::max(in.block_n * 2.0 / 1900.0, in.bs == 2 ? 0.2 : 0.33)
                              : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
   const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
@@ -208,7 +210,7 @@ double est_time_us(const Instance& in, int S, long long tiles, long long cluster
     groups = ntile * kb;
   }
   const double t_mem = b_rows * 128.0 / (bw_hbm / (double)ctas);
-  const double t_tma = (a_rows + b_rows) * 128.0 / bw_sm;
+  const double t_tma = in.bs ? 0.0 : (a_rows + b_rows) * 128.0 / bw_sm;
   const double tg = std::max(t_cad, std::max(t_mem, t_tma));
   return fixed + (double)waves * (head + (double)groups * tg + tail) + (double)(ntile - 1) * per_tile;
 }
@@ -559,9 +561,8 @@ dg_status run(int kind, const void* A, const float* sa, int ld_sa, const void* B
 
   dgk::Maps maps;
   const bool has_c = kind == dgk::kDense || kind == dgk::kKGrouped;
-  // rows of B per TMA box: the tile, half of it per CTA of a pair, or (block-
-  // scaled pair) 64 rows, two boxes per 128-column block
-  const int b_box = in.pair ? (in.bs ? 64 : in.block_n / 2) : in.block_n;
+  // rows of B per TMA box: the tile, or half of it per CTA of a pair
+  const int b_box = in.pair ? in.block_n / 2 : in.block_n;
   s = make_maps(&maps, A, sa, ld_sa, B, D, rows, kind == dgk::kMasked ? G : 1, N, K,
                 (kind == dgk::kDense || kind == dgk::kKGrouped) ? 1 : G, b_box, in.a_rows,
                 has_c ? C : nullptr, layout, kind == dgk::kKGrouped ? G : 0, sf_packed);

@@ -6,14 +6,14 @@
 namespace dgk {
 const Instance* instances_bs_mn(int* count) {
   static const Instance table[] = {
-      BsInstanceOf<128, 5, kDense, false, 3, kNN>::make(),
-      BsInstanceOf<256, 3, kDense, false, 1, kNN>::make(),
-      BsInstanceOf<128, 5, kDense, false, 3, kTN>::make(),
-      BsInstanceOf<256, 3, kDense, false, 1, kTN>::make(),
-      BsInstanceOf<128, 5, kDense, false, 3, kTT>::make(),
-      BsInstanceOf<256, 3, kDense, false, 1, kTT>::make(),
-      BsInstanceOf<128, 5, kKGrouped, false, 3, kTN>::make(),
-      BsInstanceOf<256, 3, kKGrouped, false, 1, kTN>::make(),
+      BsInstanceOf<128, 6, kDense, false, 3, kNN>::make(),
+      BsInstanceOf<256, 4, kDense, false, 1, kNN>::make(),
+      BsInstanceOf<128, 6, kDense, false, 3, kTN>::make(),
+      BsInstanceOf<256, 4, kDense, false, 1, kTN>::make(),
+      BsInstanceOf<128, 6, kDense, false, 3, kTT>::make(),
+      BsInstanceOf<256, 4, kDense, false, 1, kTT>::make(),
+      BsInstanceOf<128, 6, kKGrouped, false, 3, kTN>::make(),
+      BsInstanceOf<256, 4, kKGrouped, false, 1, kTN>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;

@@ -22,7 +22,8 @@ struct Instance {
   int pair;        // 1: CTA-pair form (cta_group::2, 256-row tiles over a 2-CTA cluster)
   int layout;      // operand storage (kNT, kNN, kTN, kTT)
   int sfp;         // 1: packed UE8M0 scales
-  int bs;          // 1: block-scaled MMA (the tensor cores apply the UE8M0 scales; no promotion)
+  int bs;          // block-scaled MMA (the tensor cores apply the UE8M0 scales; no promotion):
+                   // 0 no, else the number of MMA issuers (1 or 2)
   int nacc;        // block-scaled: tensor-memory accumulators (tiles in flight)
   int fixed_smem;  // shared memory that does not depend on the shape (bytes)
   cudaError_t (*launch)(const Maps& m, const Params& p, int grid, int cluster, int smem,
@@ -122,15 +123,15 @@ struct InstanceOf {
 namespace dgk {
 
 // A block-scaled instance: the same launch interface as InstanceOf.
-template <int BN, int STAGES, int MODE, bool PAIR, int NACC, int LAYOUT = kNT>
+template <int BN, int STAGES, int MODE, bool PAIR, int NACC, int LAYOUT = kNT, int ISS = 1>
 struct BsInstanceOf {
-  static constexpr auto kernel = fp8_gemm_bs_kernel<BN, STAGES, MODE, PAIR, NACC, LAYOUT>;
+  static constexpr auto kernel = fp8_gemm_bs_kernel<BN, STAGES, MODE, PAIR, NACC, LAYOUT, ISS>;
 
   static cudaError_t launch(const Maps& m, const Params& p, int grid, int cluster, int smem,
                             cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(BS_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -157,7 +158,7 @@ struct BsInstanceOf {
   static cudaError_t max_clusters(int cluster, int smem, int* out) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(BS_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -170,8 +171,8 @@ struct BsInstanceOf {
   }
 
   static Instance make() {
-    return Instance{BN, STAGES, 0, MODE, BLOCK_M, PAIR ? 1 : 0, LAYOUT, 1, 1, NACC,
-                    BsLayout<BN, STAGES, PAIR, NACC>::DYN_OFF + 1024, &launch, &set_smem,
+    return Instance{BN, STAGES, 0, MODE, BLOCK_M, PAIR ? 1 : 0, LAYOUT, 1, ISS, NACC,
+                    BsLayout<BN, STAGES, PAIR, NACC, ISS>::DYN_OFF + 1024, &launch, &set_smem,
                     &max_clusters};
   }
 };

@@ -457,9 +457,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (warp < 4) {
   if constexpr (REALLOC) regs_dec<REGS_CTRL>();
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer --
+  if (warp == 0 || warp == 3) {
+    // ----------------------------------------------------- TMA producers --
+    // Two threads (warps 0 and 3) share the loads: a thread that issues a TMA
+    // load stalls for ~250 cycles, so one thread issuing every K group's
+    // loads falls behind the MMA.  Each owns fixed slots (operand stages and
+    // activation-scale slots of its parity), so every slot's latest fill is
+    // its owner's, which the drain below relies on.  Both walk the whole
+    // sequence, so their ring positions agree.
     if (lane == 0 && !(p.debug_flags & DBG_SKIP_PRODUCER)) {
+      const int me = warp == 3 ? 1 : 0;
       // per slot: was a load issued, and with which phase parity
       uint32_t issued_mask = 0, issued_par = 0, sa_issued_mask = 0, sa_issued_par = 0;
       int s = 0, j = 0;
@@ -468,6 +475,37 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
         if (T.skip) continue;
         for (int g = T.kbeg; g < T.kend; ++g) {
+          if ((s & 1) != me) {   // the other producer's stage
+            if ((g - T.kbeg) % SA_GROUPS == 0) {
+              if ((j & 1) == me) {
+                // this producer's scale slot, on the other's group
+                bool sgo = wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p);
+                if constexpr (kDebug) {
+                  if (sgo && (g < 0 || (SFP ? (g >> 2) >= p.kbp : g >= p.kb))) {
+                    dbg_fail(p, ST_DEBUG_BOUNDS, abort_flag);
+                    sgo = false;
+                  }
+                  if (sgo) dbg_sa_fill[j] = dbg_sa_fill[j] + 1;
+                }
+                if (sgo) {
+                  if constexpr (SFP) {
+                    mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_PACKED_BYTES);
+                    tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j),
+                                T.m0, g >> 2, T.z);
+                  } else {
+                    mbar_arrive_expect_tx(bar(L::SA_FULL + j), L::SA_BYTES);
+                    tma_load_3d(sbase + L::SA_OFF + j * L::SA_BYTES, &tmSA, bar(L::SA_FULL + j),
+                                T.m0, g, T.z);
+                  }
+                  sa_issued_mask |= 1u << j;
+                  sa_issued_par = (sa_issued_par & ~(1u << j)) | (jph << j);
+                }
+              }
+              if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+            }
+            if (++s == STAGES) { s = 0; ph ^= 1; }
+            continue;
+          }
           bool go = wait_bar(bar(L::EMPTY + s), ph ^ 1, abort_flag, p);
           if constexpr (kDebug) {
             if (go && !dbg_tile_ok<MODE, PAIR>(p, T, g)) {
@@ -519,8 +557,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             issued_par = (issued_par & ~(1u << s)) | (ph << s);
           }
           // the scales of this and the next SA_GROUPS-1 K groups (groups past
-          // the tensor's end read as zero and are not used)
-          if ((g - T.kbeg) % SA_GROUPS == 0) {
+          // the tensor's end read as zero and are not used), if the slot is
+          // this producer's
+          if ((g - T.kbeg) % SA_GROUPS == 0 && (j & 1) != me) {
+            if (++j == SA_SLOTS) { j = 0; jph ^= 1; }
+          } else if ((g - T.kbeg) % SA_GROUPS == 0) {
             bool sgo = wait_bar(bar(L::SA_EMPTY + j), jph ^ 1, abort_flag, p);
             if constexpr (kDebug) {
               if (sgo && (g < 0 || (SFP ? (g >> 2) >= p.kbp : g >= p.kb))) {
