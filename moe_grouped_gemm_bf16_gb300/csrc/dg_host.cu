@@ -177,11 +177,11 @@ struct Plan {
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
   (void)kind; (void)n; (void)num_groups;
-  // block-scaled: the slower of the MMA (2 cycles per column per K group at
-  // ~1.9 GHz) and the issuing thread's loop per K group (~620 cycles with
-  // one issuer, measured; two issuers share it)
-  const double t_cad = in.bs ? std::max(in.block_n * 2.0 / 1900.0, in.bs == 2 ? 0.2 : 0.33)
-                             : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
+  // block-scaled: ~0.46 us per K group and CTA (per CTA pair for the pair
+  // form) for every tile width, one or two issuers (measured on the prefill
+  // and contiguous shapes: the TMA writes and the MMAs' operand reads share
+  // the SM's shared-memory bandwidth); the MMA alone would take 0.13-0.27 us
+  const double t_cad = in.bs ? 0.46 : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
   const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
   // a block-scaled kernel with one accumulator waits for each tile's epilogue

@@ -12,6 +12,8 @@ const Instance* instances_dense(int* count) {
       InstanceOf<256, 5, true, kDense, 64>::make(),
       InstanceOf<256, 4, false, kDense, 128, true>::make(),
       InstanceOf<128, 6, false, kDense, 128, true>::make(),
+      InstanceOf<64, 8, false, kDense>::make(),
+      InstanceOf<64, 8, true, kDense>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;

@@ -32,8 +32,8 @@ def dense_ref(p):
 
 
 # (block_n, split_k): every dense instance, plus the heuristic (0, 0)
-DENSE_CONFIGS = [(0, 0), (128, 1), (256, 1), (128, 2), (128, 3), (128, 4), (128, 8), (256, 2),
-                 (256, 5), (256, 8)]
+DENSE_CONFIGS = [(0, 0), (64, 1), (128, 1), (256, 1), (64, 3), (128, 2), (128, 3), (128, 4),
+                 (128, 8), (256, 2), (256, 5), (256, 8)]
 
 
 @pytest.mark.parametrize("cfg", DENSE_CONFIGS, ids=lambda c: f"bn{c[0]}_s{c[1]}")
@@ -56,7 +56,8 @@ RAGGED = [
 
 
 @pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("cfg", [(0, 0), (128, 1), (256, 1), (128, 3), (256, 3)],
+@pytest.mark.parametrize("cfg", [(0, 0), (64, 1), (128, 1), (256, 1), (64, 4), (128, 3),
+                                 (256, 3)],
                          ids=lambda c: f"bn{c[0]}_s{c[1]}")
 def test_dense_ragged(shape, cfg):
     M, N, K = shape
