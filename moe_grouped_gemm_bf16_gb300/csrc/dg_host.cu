@@ -138,9 +138,10 @@ Table table_for(int tid) {
 }
 
 int smem_for(const Instance& in, int kb, int num_groups) {
-  // the promotion kernels keep a tile's B scales in shared memory; the
-  // block-scaled ones read them into the scale-factor staging instead
-  int s = in.fixed_smem + (in.bs ? 0 : 3 * kb * 4) +
+  // the promotion kernels keep two tiles' B scales in shared memory (one
+  // buffer filled while the other is read); the block-scaled ones read them
+  // into the scale-factor staging instead
+  int s = in.fixed_smem + (in.bs ? 0 : 2 * 3 * kb * 4) +
           (in.mode == dgk::kMasked     ? (2 * num_groups + 1) * 4
            : in.mode == dgk::kKGrouped ? (num_groups + 1) * 4
                                        : 0);

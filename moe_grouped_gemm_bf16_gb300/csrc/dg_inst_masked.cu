@@ -7,6 +7,7 @@ const Instance* instances_masked(int* count) {
   static const Instance table[] = {
       InstanceOf<128, 5, false, kMasked>::make(),
       InstanceOf<256, 3, false, kMasked>::make(),
+      InstanceOf<64, 8, false, kMasked>::make(),
       // CTA pairs: 256-row M blocks, each CTA loading half of the B tile
       InstanceOf<256, 4, false, kMasked, 128, true>::make(),
       InstanceOf<128, 6, false, kMasked, 128, true>::make(),

@@ -71,7 +71,8 @@ struct SmemLayout {
   static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
                        T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
-                       MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, NUM_BARS = C_FULL + 1;
+                       MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, SB_FULL = C_FULL + 1,
+                       NUM_BARS = SB_FULL + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
   // checked build: fill counters of the operand ring's and the scale ring's slots
   static constexpr int DBG_OFF = MISC_OFF + 16;
@@ -89,7 +90,7 @@ struct SmemLayout {
 template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false>
 __host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
   return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF +
-         3 * kb * 4 +
+         2 * 3 * kb * 4 +
          (mode == kMasked ? (2 * num_groups + 1) * 4 : mode == kKGrouped ? (num_groups + 1) * 4 : 0);
 }
 
@@ -309,8 +310,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile uint32_t* abort_flag = misc + 1;
+  // B scales of a tile, two buffers of [3][kb] (one filled while the other is read)
   float* sb_s = reinterpret_cast<float*>(smem + L::DYN_OFF);
-  int* prefix = reinterpret_cast<int*>(sb_s + 3 * p.kb);
+  int* prefix = reinterpret_cast<int*>(sb_s + 6 * p.kb);
   int* mcnt = prefix + p.num_groups + 1;
   const float* sa_ring = reinterpret_cast<const float*>(smem + L::SA_OFF);
   // checked build: fills of each operand-ring slot, then of each scale-ring slot
@@ -348,6 +350,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init(bar(L::READY), S);
     mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
     mbar_init(bar(L::C_FULL), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar(L::SB_FULL + i), 32 * NUM_PROMO_WARPS);
     misc[1] = 0;
     if constexpr (kDebug)
       for (int i = 0; i < STAGES + SA_SLOTS; ++i) dbg_fill[i] = 0;
@@ -696,6 +699,35 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t k_iter = 0;                // tiles finished (phase of the reduction barriers)
     uint32_t cph = 0;                   // phase of the addend's barrier
     float acc[HALF];
+    // B scales: a tile's scale i (i < 3 * its K groups) is 128-column block
+    // i / groups, K group i % groups (packed form: the word holding that
+    // group's byte, decoded where it is read).  They are copied (cp.async, 4
+    // bytes each) into one of two buffers while the previous tile is
+    // promoted, completing on that buffer's mbarrier (one arrival per
+    // promotion thread); a load issued at the tile's start would hold up its
+    // first promotion by the load's latency.
+    auto sb_issue = [&](int tt, uint32_t buf) {
+      const Tile U = decode_tile<BN, MODE, PAIR>(tt, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
+      if (!U.skip) {
+        const int tku = U.kend - U.kbeg;
+        float* dst = sb_s + buf * 3 * p.kb;
+        for (int i = pt; i < 3 * tku; i += 32 * NUM_PROMO_WARPS) {
+          const int jb = i / tku, gg = i - jb * tku;
+          const int nbk = min((U.n0 >> 7) + jb, p.nb - 1);
+          const void* src;
+          if constexpr (SFP)
+            src = reinterpret_cast<const uint32_t*>(p.sb) +
+                  (static_cast<size_t>(U.e) * p.nb + nbk) * p.kbp + ((U.kbeg + gg) >> 2);
+          else
+            src = p.sb + (static_cast<size_t>(U.e) * p.nb + nbk) * p.kb + U.kbeg + gg;
+          cp_async_4(smem_u32(dst + i), src);
+        }
+      }
+      cp_async_mbar_arrive_noinc(bar(L::SB_FULL + buf));
+    };
+    uint32_t sbi = 0;                   // buffer of the current tile's B scales
+    uint32_t sbph = 0;                  // phase bit of each buffer's barrier
+    if (cluster_id < num_tiles) sb_issue(cluster_id, 0);
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
       // Dense form with an addend (D = C + A B^T): thread 0 loads this tile's C
@@ -716,25 +748,22 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tma_load_3d(out_s + cc * (BLOCK_M * 64), &tmC, bar(L::C_FULL), T.n0 + cc * 32, T.m0,
                         T.zd);
       };
-      if (load_c && g_c < 0) issue_c();
-      // B scales of the tile's (up to 3) 128-column blocks, for this CTA's K groups
-      named_bar_sync(1, 32 * NUM_PROMO_WARPS);
-      if (!T.skip) {
-        const int blk0 = T.n0 >> 7;
-        for (int i = pt; i < 3 * tk; i += 32 * NUM_PROMO_WARPS) {
-          const int jb = i / tk, gg = i - jb * tk;
-          const int nbk = min(blk0 + jb, p.nb - 1);
-          if constexpr (SFP) {
-            const int gk = T.kbeg + gg;
-            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.sb) +
-                                     (static_cast<size_t>(T.e) * p.nb + nbk) * p.kbp + (gk >> 2));
-            sb_s[i] = ue8m0_scale(w, gk);
-          } else {
-            sb_s[i] = __ldg(p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb + T.kbeg + gg);
-          }
-        }
+      // this tile's B scales (every promotion thread's copies have landed);
+      // the other buffer, last read by the previous tile, which every thread
+      // has finished, takes the next tile's
+      const float* sbt = sb_s + sbi * 3 * p.kb;
+      wait_bar(bar(L::SB_FULL + sbi), (sbph >> sbi) & 1u, abort_flag, p);
+      sbph ^= 1u << sbi;
+      if (t + tile_stride < num_tiles) sb_issue(t + tile_stride, sbi ^ 1u);
+      sbi ^= 1u;
+      if ((MODE == kDense || MODE == kKGrouped) && !SPLIT && p.C != nullptr) {
+        // with an addend, the staging tile receives C during this tile: every
+        // store of the previous tile (several warps issue them, each waiting
+        // for its own) must have read it first
+        if (lane == 0) bulk_wait_group_read0();
+        named_bar_sync(1, 32 * NUM_PROMO_WARPS);
+        if (load_c && g_c < 0) issue_c();
       }
-      named_bar_sync(1, 32 * NUM_PROMO_WARPS);
 #pragma unroll
       for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
       if (!T.skip) {
@@ -770,7 +799,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                                BLOCK_M + row], g);
           else
             a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
-          const float* sbg = sb_s + (g - T.kbeg);
+          const float* sbg = sbt + (g - T.kbeg);
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
           // every outstanding load, so fewer, larger batches expose its latency
@@ -793,7 +822,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               const int c = bt * LB + u;
               const int col = h * HALF + c * 32;
               // the 32 columns lie in one 128-column B scale block
-              const float sc = a_s * sbg[((nmod + col) >> 7) * tk];
+              const float sb_v = sbg[((nmod + col) >> 7) * tk];
+              const float sc = a_s * (SFP ? ue8m0_scale(__float_as_uint(sb_v), g) : sb_v);
 #pragma unroll
               for (int i = 0; i < 32; i += 2)
                 ffma2(acc[c * 32 + i], acc[c * 32 + i + 1], __uint_as_float(v[u][i]),
@@ -838,7 +868,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             cph ^= 1;
           }
         }
-        if (pt == 0) bulk_wait_group_read0();  // the previous store has read the staging tile
+        // the previous tile's stores (one or more per warp) have read the staging tile
+        if (lane == 0) bulk_wait_group_read0();
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         // staging: BN/32 chunks of [128 rows x 64 B], 64-byte swizzle (16-byte
         // unit u of row r sits at unit u ^ ((r >> 1) & 3)), as the store's
@@ -870,9 +901,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         fence_proxy_async_smem();
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
         if (MODE != kMasked || T.rows == BLOCK_M) {
-          // the store clips at the tensor's bounds (M rows, N columns)
-          if (pt == 0 && !*abort_flag && T.rows > 0) {
-            for (int cc = 0; cc < BN / 32; ++cc)
+          // the store clips at the tensor's bounds (M rows, N columns).  Chunk
+          // cc is stored by warp cc % NUM_PROMO_WARPS: a thread that issues a
+          // TMA store stalls for a few hundred cycles, and one thread issuing
+          // all of them would hold every promotion warp at the next tile's
+          // first barrier.
+          if (lane == 0 && !*abort_flag && T.rows > 0) {
+            for (int cc = pw; cc < BN / 32; cc += NUM_PROMO_WARPS)
               if (T.n0 + cc * 32 < p.N)
                 tma_store_3d(&tmD, out_s + cc * (BLOCK_M * 64), T.n0 + cc * 32, T.m0, T.zd);
             bulk_commit_group();
@@ -1013,7 +1048,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (!red_ok) drain_wait(bar(L::RED_FULL), 0, p);
       }
     }  // tile loop
-    if (pt == 0) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();
+    cp_async_wait_all();   // (after an abort, scale copies may still be in flight)
     __syncwarp();
   }
 

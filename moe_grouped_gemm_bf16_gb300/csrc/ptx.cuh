@@ -102,6 +102,22 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
       : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (no register holds the value in
+// flight); completion is tracked through an mbarrier (below).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The mbarrier counts one arrival of this thread once all of its earlier
+// cp.async copies have landed (the arrival is part of the expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
