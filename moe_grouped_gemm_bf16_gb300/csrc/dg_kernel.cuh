@@ -72,12 +72,16 @@ struct SmemLayout {
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
                        T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
                        MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, SB_FULL = C_FULL + 1,
-                       NUM_BARS = SB_FULL + 2;
-  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
+                       SB_EMPTY = SB_FULL + 2, NUM_BARS = SB_EMPTY + 2;
+  // [0] TMEM base, [1] abort flag
+  static constexpr int MISC_OFF = (BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
   // checked build: fill counters of the operand ring's and the scale ring's slots
   static constexpr int DBG_OFF = MISC_OFF + 16;
   static constexpr int DBG_BYTES = kDebug ? ((STAGES + SA_SLOTS) * 4 + 15) / 16 * 16 : 0;
-  static constexpr int DYN_OFF = DBG_OFF + DBG_BYTES;      // sb tile, then masked tables
+  // the B scale buffers (bulk-copy destinations: 16-byte aligned), then the
+  // masked / K-grouped tables
+  static constexpr int DYN_OFF = DBG_OFF + DBG_BYTES;
+  static_assert(DYN_OFF % 16 == 0, "B scale buffers need 16-byte alignment");
   static_assert(B_OFF % 1024 == 0 && SA_OFF % 1024 == 0 && OUT_OFF % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   // TMEM accumulators (K groups the MMA may run ahead of the promotion warps):
@@ -328,6 +332,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // this CTA's K groups: a slice of them in the split form, all of them otherwise
   // (the pair form's cluster rank names a half of the tile, not of K)
   const uint32_t krank = SPLIT ? crank : 0;
+  // A tile's B scales come either from the producer (one bulk copy per
+  // 128-column block: whole 16-byte aligned rows of fp32 scales, i.e. no K
+  // split, no K-grouped form, K/128 a multiple of 4) or, otherwise, from the
+  // promotion threads' own 4-byte copies.  Either way they land in one of two
+  // buffers while the previous tile is promoted.
+  const bool sb_bulk = !SPLIT && !SFP && MODE != kKGrouped && (p.kb & 3) == 0 &&
+                       (reinterpret_cast<uintptr_t>(p.sb) & 15) == 0;
   const int kbeg = static_cast<int>(static_cast<long long>(krank) * p.kb / S);
   const int kend = static_cast<int>(static_cast<long long>(krank + 1) * p.kb / S);
 
@@ -350,7 +361,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init(bar(L::READY), S);
     mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
     mbar_init(bar(L::C_FULL), 1);
-    for (int i = 0; i < 2; ++i) mbar_init(bar(L::SB_FULL + i), 32 * NUM_PROMO_WARPS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::SB_FULL + i), sb_bulk ? 1 : 32 * NUM_PROMO_WARPS);
+      mbar_init(bar(L::SB_EMPTY + i), NUM_PROMO_WARPS);
+    }
     misc[1] = 0;
     if constexpr (kDebug)
       for (int i = 0; i < STAGES + SA_SLOTS; ++i) dbg_fill[i] = 0;
@@ -474,8 +488,32 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t issued_mask = 0, issued_par = 0, sa_issued_mask = 0, sa_issued_par = 0;
       int s = 0, j = 0;
       uint32_t ph = 0, jph = 0;
+      uint32_t sbb = 0, sb_eph = 0, sb_issued = 0, sb_par = 0;   // B scale buffers (bulk form)
       for (int t = cluster_id; t < num_tiles; t += tile_stride) {
         const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
+        if (sb_bulk && me == 0) {
+          // the tile's B scales: rows of the (up to 3) 128-column blocks, once
+          // the promotion threads are done with the buffer's previous tile
+          if (wait_bar(bar(L::SB_EMPTY + sbb), ((sb_eph >> sbb) & 1u) ^ 1u, abort_flag, p)) {
+            if (T.skip) {
+              mbar_arrive(bar(L::SB_FULL + sbb));
+            } else {
+              const uint32_t row_bytes = static_cast<uint32_t>(p.kb) * 4u;
+              mbar_arrive_expect_tx(bar(L::SB_FULL + sbb), 3u * row_bytes);
+              const uint32_t dst = smem_u32(sb_s + sbb * 3 * p.kb);
+              for (int jb = 0; jb < 3; ++jb) {
+                const int nbk = min((T.n0 >> 7) + jb, p.nb - 1);
+                bulk_load_g2s(dst + jb * row_bytes,
+                              p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb, row_bytes,
+                              bar(L::SB_FULL + sbb));
+              }
+              sb_issued |= 1u << sbb;
+              sb_par = (sb_par & ~(1u << sbb)) | (((sb_eph >> sbb) & 1u) << sbb);
+            }
+          }
+          sb_eph ^= 1u << sbb;
+          sbb ^= 1u;
+        }
         if (T.skip) continue;
         for (int g = T.kbeg; g < T.kend; ++g) {
           if ((s & 1) != me) {   // the other producer's stage
@@ -601,6 +639,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           drain_wait(bar(L::FULL + q), (issued_par >> q) & 1u, p);
       for (int q = 0; q < SA_SLOTS; ++q)
         if ((sa_issued_mask >> q) & 1u) drain_wait(bar(L::SA_FULL + q), (sa_issued_par >> q) & 1u, p);
+      for (int q = 0; q < 2; ++q)
+        if ((sb_issued >> q) & 1u) drain_wait(bar(L::SB_FULL + q), (sb_par >> q) & 1u, p);
     }
     __syncwarp();
   } else if (warp <= NUM_ISSUERS) {
@@ -704,9 +744,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // group's byte, decoded where it is read).  They are copied (cp.async, 4
     // bytes each) into one of two buffers while the previous tile is
     // promoted, completing on that buffer's mbarrier (one arrival per
-    // promotion thread); a load issued at the tile's start would hold up its
-    // first promotion by the load's latency.
+    // promotion thread, signalled after the tile's last K group: the arrival
+    // instruction held the issuing warp until its copies had landed); a load
+    // issued at the tile's start would hold up its first promotion by the
+    // load's latency.
     auto sb_issue = [&](int tt, uint32_t buf) {
+      if (sb_bulk) return;
       const Tile U = decode_tile<BN, MODE, PAIR>(tt, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
       if (!U.skip) {
         const int tku = U.kend - U.kbeg;
@@ -723,11 +766,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           cp_async_4(smem_u32(dst + i), src);
         }
       }
-      cp_async_mbar_arrive_noinc(bar(L::SB_FULL + buf));
     };
     uint32_t sbi = 0;                   // buffer of the current tile's B scales
     uint32_t sbph = 0;                  // phase bit of each buffer's barrier
-    if (cluster_id < num_tiles) sb_issue(cluster_id, 0);
+    if (cluster_id < num_tiles && !sb_bulk) {
+      sb_issue(cluster_id, 0);
+      cp_async_mbar_arrive_noinc(bar(L::SB_FULL + 0));
+    }
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
       const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
       // Dense form with an addend (D = C + A B^T): thread 0 loads this tile's C
@@ -754,7 +799,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const float* sbt = sb_s + sbi * 3 * p.kb;
       wait_bar(bar(L::SB_FULL + sbi), (sbph >> sbi) & 1u, abort_flag, p);
       sbph ^= 1u << sbi;
-      if (t + tile_stride < num_tiles) sb_issue(t + tile_stride, sbi ^ 1u);
+      const bool sb_next = t + tile_stride < num_tiles;
+      if (sb_next) sb_issue(t + tile_stride, sbi ^ 1u);
       sbi ^= 1u;
       if ((MODE == kDense || MODE == kKGrouped) && !SPLIT && p.C != nullptr) {
         // with an addend, the staging tile receives C during this tile: every
@@ -843,6 +889,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (++b == L::NBUF) { b = 0; bph ^= 1; }
           if (load_c && g == g_c) issue_c();
         }
+      }
+      if (sb_bulk) {
+        // (this tile's buffer is the other one now)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::SB_EMPTY + (sbi ^ 1u)));
+      } else if (sb_next) {
+        cp_async_mbar_arrive_noinc(bar(L::SB_FULL + sbi));
       }
       if constexpr (!SPLIT) {
         // ------------------------------------ epilogue: bf16 via TMA store --
