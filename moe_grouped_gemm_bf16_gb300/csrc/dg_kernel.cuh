@@ -495,6 +495,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // the tile's B scales: rows of the (up to 3) 128-column blocks, once
           // the promotion threads are done with the buffer's previous tile
           if (wait_bar(bar(L::SB_EMPTY + sbb), ((sb_eph >> sbb) & 1u) ^ 1u, abort_flag, p)) {
+            // (the drain below waits for the buffer's latest phase, which a
+            // padding tile's plain arrival completes as well)
+            sb_issued |= 1u << sbb;
+            sb_par = (sb_par & ~(1u << sbb)) | (((sb_eph >> sbb) & 1u) << sbb);
             if (T.skip) {
               mbar_arrive(bar(L::SB_FULL + sbb));
             } else {
@@ -507,8 +511,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                               p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb, row_bytes,
                               bar(L::SB_FULL + sbb));
               }
-              sb_issued |= 1u << sbb;
-              sb_par = (sb_par & ~(1u << sbb)) | (((sb_eph >> sbb) & 1u) << sbb);
             }
           }
           sb_eph ^= 1u << sbb;

@@ -277,3 +277,32 @@ def test_dense_add_c_in_place(cfg):
     with U.forced_config(cfg[0], cfg[1], pair=cfg[2]):
         got = U.run_dense_add_c(p, C, inplace=True)
     U.assert_close(got, ORC.gemm_nt_c(p["A"], p["sa"], p["B"], p["sb"], C), f"in place {cfg}")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_contiguous_padding_tiles_last_on_few_sms(bn):
+    """A whole padding block at the end, on 3 CTAs: each CTA's last tiles are
+    padding tiles, which reuse a B-scale buffer with a plain barrier arrival
+    after its last real fill; the CTA's final drain must still see every
+    phase complete (no timeout in the status word)."""
+    p = W.contiguous_problem(3, 272, 512, 1, 300, seed=231)
+    M = p["M"]
+    p = dict(p)
+    p["A"] = np.concatenate([p["A"], W.random_codes((256, p["K"]), 5)])
+    sa = np.ones((p["K"] // 128, W.tma_aligned_ld(M + 256)), np.float32)
+    sa[:, :M] = p["sa"][:, :M]
+    p["sa"] = sa
+    p["m_indices"] = np.concatenate([p["m_indices"], np.full(256, -1, np.int32)])
+    p["M"] = M + 256
+    dg.get_device_status()   # read and clear
+    dg.set_num_sms(3)
+    try:
+        with U.forced_config(bn, 1):
+            got = U.run_contiguous(p)
+    finally:
+        dg.set_num_sms(0)
+    assert dg.get_device_status() == 0
+    want = ORC.grouped_contiguous(p["A"], p["sa"], p["B"], p["sb"], p["m_indices"])
+    pad = p["m_indices"] < 0
+    assert np.all(got[pad] == 0)
+    U.assert_close(got[~pad], want[~pad], f"contiguous padding last bn={bn}")
