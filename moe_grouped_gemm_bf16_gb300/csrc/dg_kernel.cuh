@@ -28,7 +28,7 @@
 //               overview deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
 //               Then the bf16 epilogue: a swizzled staging tile stored by TMA,
 //               or, when the K groups are split over a cluster, a fixed-order
-//               reduction of partials pushed through distributed shared memory.
+//               reduction of partials read through distributed shared memory.
 //
 // Every mbarrier wait is bounded: when one gives up it records a timeout in
 // the device status word and sets a CTA-wide abort flag, after which every
@@ -63,14 +63,14 @@ struct SmemLayout {
   // computes one tile, so after its last K group the operand ring is idle and
   // holds the fp32 partial of the reduction instead.
   static constexpr int OUT_OFF = SPLIT ? A_OFF : SA_OFF + SA_SLOTS * SA_BYTES;
-  // split: own partial [128][BN] fp32 + received slices [S][ceil(rows/S)][BN] fp32
-  static constexpr int OUT_BYTES = SPLIT ? (2 * AROWS + MAX_SPLIT) * BN * 4 : BLOCK_M * BN * 2;
+  // split: the CTA's fp32 partial [AROWS][BN], which the cluster's owners read
+  static constexpr int OUT_BYTES = SPLIT ? AROWS * BN * 4 : BLOCK_M * BN * 2;
   static_assert(!SPLIT || OUT_BYTES <= STAGES * (A_BYTES + B_BYTES), "partials must fit the ring");
   static constexpr int BAR_OFF = SPLIT ? SA_OFF + SA_SLOTS * SA_BYTES : OUT_OFF + OUT_BYTES;
   // barrier indexes
   static constexpr int FULL = 0, EMPTY = STAGES, SA_FULL = 2 * STAGES,
                        SA_EMPTY = 2 * STAGES + SA_SLOTS, T_FULL = 2 * STAGES + 2 * SA_SLOTS,
-                       T_EMPTY = T_FULL + 4, RED_FULL = T_EMPTY + 4, READY = RED_FULL + 1,
+                       T_EMPTY = T_FULL + 4, READY = T_EMPTY + 4,
                        MMA_DONE = READY + 1, C_FULL = MMA_DONE + 1, SB_FULL = C_FULL + 1,
                        SB_EMPTY = SB_FULL + 2, NUM_BARS = SB_EMPTY + 2;
   // [0] TMEM base, [1] abort flag
@@ -357,7 +357,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       // pair form: the leader's barrier counts both CTAs' promotion warps
       mbar_init(bar(L::T_EMPTY + b), PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
     }
-    mbar_init(bar(L::RED_FULL), 1);
     mbar_init(bar(L::READY), S);
     mbar_init(bar(L::MMA_DONE), NUM_ISSUERS);
     mbar_init(bar(L::C_FULL), 1);
@@ -385,10 +384,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tmem_relinquish();
     }
   }
+  // Dense nt form: ask L2 for the B boxes of this CTA's first two K groups
+  // while the previous kernel in the stream may still run (a CTA that starts
+  // early, on an SM that kernel left free, would otherwise only wait).  A
+  // prefetch delivers nothing to this CTA and L2 is where all writes meet, so
+  // it cannot hand out stale data even if the previous kernel writes B; the
+  // loads themselves still come after the wait below.  (A cold first load
+  // measured 2-3 us after the wait in back-to-back decode GEMMs.)
+  if (MODE == kDense && LAYOUT == kNT && !PAIR && warp == 0 && lane == 0 &&
+      cluster_id < p.num_m_blocks * p.num_n_blocks) {
+    const Tile T0 = decode_tile<BN, MODE, PAIR>(cluster_id, p, p.num_m_blocks, nullptr, nullptr,
+                                                kbeg, kend, crank);
+    for (int g = T0.kbeg; g < T0.kend && g < T0.kbeg + 2; ++g)
+      tma_prefetch_3d(&tmB, g * BLOCK_K, T0.n0, T0.e);
+  }
   // Everything above touched only shared memory, tensor memory and the kernel
-  // parameters; global memory (which the previous kernel in the stream may
-  // still be writing) is read only after this wait.  Dependent launches may
-  // start their own prologue from here on.
+  // parameters (and asked L2 for B, above); global memory (which the previous
+  // kernel in the stream may still be writing) is read only after this wait.
+  // Dependent launches may start their own prologue from here on.
   grid_dep_wait();
   grid_dep_launch_dependents();
   if (MODE == kMasked && warp == 2) {  // (warp 2 has no other set-up work)
@@ -993,18 +1006,20 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // Each CTA owns a slice of R = ceil(rows / S) tile rows.  A CTA stages
         // its fp32 partial rows in its (now idle) operand ring, 16-byte unit u
         // of row r at unit u ^ (r & 7) (conflict-free row-per-thread writes),
-        // then one thread sends every other owner its slice with a bulk copy
-        // into that owner's receive area (slot [sender rank][row in slice]),
-        // completing bytes on the owner's RED_FULL; an owner reads its own
-        // slice where it was staged.  The owner sums the S slices in rank
-        // order and stores bf16.  READY (S arrivals) tells every CTA that all
-        // rings are idle, so receive areas may be written.
+        // and tells every CTA of the cluster so (READY, S arrivals, released
+        // at cluster scope after a CTA barrier over the staging writes).  An
+        // owner then reads its slice's rows from every CTA's staged partial
+        // (its own locally, the others' through distributed shared memory),
+        // sums them in rank order and stores bf16.  No CTA leaves before the
+        // cluster's final rendezvous, so the partials stay readable until
+        // every owner is done.  (Pushing the slices with bulk copies into
+        // receive areas first took 1-2.8 us for the copies alone on the decode
+        // shapes.)
         const int R = (T.rows + S - 1) / S;
         const int own_r0 = static_cast<int>(crank) * R;
         const int own_rows = max(0, min(T.rows, own_r0 + R) - own_r0);
         constexpr int ROWB = BN * 4;                       // bytes of one fp32 row
         const uint32_t stage_s = out_s;                    // [rows <= AROWS][BN] own partial
-        const uint32_t recv_s = out_s + AROWS * ROWB;      // [S][R][BN] received slices
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);           // this CTA's ring is idle
         if (row < T.rows) {
 #pragma unroll
@@ -1015,92 +1030,99 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                          __float_as_uint(acc[4 * c + 3]));
           }
         }
-        fence_proxy_async_smem();  // the bulk copies read what this thread wrote
         named_bar_sync(1, 32 * NUM_PROMO_WARPS);
-        if (pt == 0) {
-          mbar_arrive_expect_tx(bar(L::RED_FULL), static_cast<uint32_t>((S - 1) * own_rows * ROWB));
-          // a signal only: the ring's idleness was already observed through
-          // the mbarriers of its last loads and MMAs
-          for (int r = 0; r < S; ++r) mbar_arrive_remote_relaxed(bar(L::READY), r);
-        }
+        if (pt == 0)
+          for (int r = 0; r < S; ++r) mbar_arrive_remote_release(bar(L::READY), r);
         wait_bar<true>(bar(L::READY), 0, abort_flag, p);
         __syncwarp();
-        if (pt == 0) {
-          for (int o = 0; o < S; ++o) {
-            const int rows_o = max(0, min(T.rows, (o + 1) * R) - o * R);
-            if (rows_o == 0 || o == static_cast<int>(crank)) continue;
-            bulk_copy_to_cluster(map_cluster(recv_s + static_cast<uint32_t>(crank) * R * ROWB, o),
-                                 stage_s + o * R * ROWB, static_cast<uint32_t>(rows_o * ROWB),
-                                 map_cluster(bar(L::RED_FULL), o));
-          }
-        }
-        const bool red_ok = wait_bar(bar(L::RED_FULL), 0, abort_flag, p);
-        __syncwarp();
         constexpr int UPR = BN / 4;  // 16-byte units per row
-        // addend C (D = C + A B^T): this thread's C values for all its units
-        // are loaded before the sums, so their latencies overlap (an owner's
-        // slice has at most AROWS rows)
-        constexpr int MAX_IT = (AROWS * UPR + 32 * NUM_PROMO_WARPS - 1) / (32 * NUM_PROMO_WARPS);
-        uint2 cpre[MAX_IT];
-#pragma unroll
-        for (int it = 0; it < MAX_IT; ++it) {
-          const int i = pt + it * 32 * NUM_PROMO_WARPS;
-          cpre[it] = make_uint2(0, 0);
-          if (p.C != nullptr && i < own_rows * UPR) {
-            const int rr = i / UPR, cu = i - rr * UPR;
-            const int n = T.n0 + cu * 4;
-            if (n < p.N)
-              cpre[it] = __ldg(reinterpret_cast<const uint2*>(
-                  p.C + static_cast<size_t>(T.m0 + own_r0 + rr) * p.N + n));
-          }
-        }
-#pragma unroll
-        for (int it = 0; it < MAX_IT; ++it) {
-          const int i = pt + it * 32 * NUM_PROMO_WARPS;
-          if (i >= own_rows * UPR) break;
+        constexpr int NPT_S = 32 * NUM_PROMO_WARPS;
+        // An owner's slice has at most ceil(AROWS / 2) rows (S >= 2); the
+        // units of a slice go to the threads in turn, MAX_IT per thread in
+        // registers (a larger slice, S = 1, finishes in the loop after).
+        constexpr int MAX_IT = ((AROWS + 1) / 2 * UPR + NPT_S - 1) / NPT_S;
+        const int n_units = own_rows * UPR;
+        // this thread's unit i: row rr of the slice, 16-byte unit cu; its
+        // offset in a staged partial (same in every CTA)
+        auto unit_off = [&](int i) -> uint32_t {
           const int rr = i / UPR, cu = i - rr * UPR;
           const int grow = own_r0 + rr;  // row in the tile (its swizzle key)
-          const uint32_t off = static_cast<uint32_t>(rr * ROWB + ((cu ^ (grow & 7)) << 4));
-          float4 v[MAX_SPLIT];
-#pragma unroll
-          for (int r = 0; r < MAX_SPLIT; ++r)
-            if (r < S) {
-              // the own slice where it was staged, the others in their receive slots
-              const uint32_t base = r == static_cast<int>(crank)
-                                        ? stage_s + static_cast<uint32_t>(own_r0 * ROWB)
-                                        : recv_s + static_cast<uint32_t>(r * R * ROWB);
-              const uint4 w = ld_shared_v4(base + off);
-              v[r] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                                 __uint_as_float(w.w));
-            }
-          float4 sum = v[0];
-#pragma unroll
-          for (int r = 1; r < MAX_SPLIT; ++r)
-            if (r < S) {
-              sum.x += v[r].x; sum.y += v[r].y; sum.z += v[r].z; sum.w += v[r].w;
-            }
-          if (p.C != nullptr) {
-            sum.x += __uint_as_float(cpre[it].x << 16);
-            sum.y += __uint_as_float(cpre[it].x & 0xFFFF0000u);
-            sum.z += __uint_as_float(cpre[it].y << 16);
-            sum.w += __uint_as_float(cpre[it].y & 0xFFFF0000u);
-          }
+          return static_cast<uint32_t>(grow * ROWB + ((cu ^ (grow & 7)) << 4));
+        };
+        // bf16 of sum (+ C) for unit i, stored to D
+        auto store_unit = [&](int i, float4 sum) {
+          const int rr = i / UPR, cu = i - rr * UPR;
+          const int grow = own_r0 + rr;
           const int n = T.n0 + cu * 4;
+          if (n >= p.N) return;
+          if (p.C != nullptr) {
+            const uint2 c = __ldg(reinterpret_cast<const uint2*>(
+                p.C + static_cast<size_t>(T.m0 + grow) * p.N + n));
+            sum.x += __uint_as_float(c.x << 16);
+            sum.y += __uint_as_float(c.x & 0xFFFF0000u);
+            sum.z += __uint_as_float(c.y << 16);
+            sum.w += __uint_as_float(c.y & 0xFFFF0000u);
+          }
           if constexpr (kDebug) {
-            if (n < p.N && T.m0 + grow >= p.M) {
+            if (T.m0 + grow >= p.M) {
               raise_status(p, ST_DEBUG_BOUNDS);
-              continue;
+              return;
             }
           }
-          if (n < p.N && !*abort_flag) {
+          if (!*abort_flag) {
             uint2 w;
             w.x = pack_bf16x2(sum.x, sum.y);
             w.y = pack_bf16x2(sum.z, sum.w);
             *reinterpret_cast<uint2*>(p.D + static_cast<size_t>(T.m0 + grow) * p.N + n) = w;
           }
+        };
+        // The S partials are added in rank order (deterministic), rank by
+        // rank over all of this thread's units, so that each rank's loads
+        // (local, or from a peer through distributed shared memory) are in
+        // flight together.
+        const uint8_t* stage_g = smem + L::OUT_OFF;     // this CTA's staged partial
+        float4 sum[MAX_IT];
+        for (int r = 0; r < S; ++r) {
+          const uint8_t* src =
+              r == static_cast<int>(crank)
+                  ? stage_g
+                  : static_cast<const uint8_t*>(__cluster_map_shared_rank(
+                        const_cast<uint8_t*>(stage_g), static_cast<unsigned>(r)));
+#pragma unroll
+          for (int it = 0; it < MAX_IT; ++it) {
+            const int i = pt + it * NPT_S;
+            if (i < n_units) {
+              const float4 v = *reinterpret_cast<const float4*>(src + unit_off(i));
+              if (r == 0) {
+                sum[it] = v;
+              } else {
+                sum[it].x += v.x; sum[it].y += v.y; sum[it].z += v.z; sum[it].w += v.w;
+              }
+            }
+          }
         }
-        // after an abort: every byte sent to this CTA lands before it may exit
-        if (!red_ok) drain_wait(bar(L::RED_FULL), 0, p);
+#pragma unroll
+        for (int it = 0; it < MAX_IT; ++it) {
+          const int i = pt + it * NPT_S;
+          if (i < n_units) store_unit(i, sum[it]);
+        }
+        for (int i = pt + MAX_IT * NPT_S; i < n_units; i += NPT_S) {
+          float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int r = 0; r < S; ++r) {
+            const uint8_t* src =
+                r == static_cast<int>(crank)
+                    ? stage_g
+                    : static_cast<const uint8_t*>(__cluster_map_shared_rank(
+                          const_cast<uint8_t*>(stage_g), static_cast<unsigned>(r)));
+            const float4 v = *reinterpret_cast<const float4*>(src + unit_off(i));
+            if (r == 0) {
+              acc4 = v;
+            } else {
+              acc4.x += v.x; acc4.y += v.y; acc4.z += v.z; acc4.w += v.w;
+            }
+          }
+          store_unit(i, acc4);
+        }
       }
     }  // tile loop
     if (lane == 0) bulk_wait_group0();
