@@ -187,7 +187,10 @@ double est_time_us(const Instance& in, int S, long long tiles, long long cluster
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
   // a block-scaled kernel with one accumulator waits for each tile's epilogue
   // to read it before the next tile's MMAs
-  const double head = 3.06, tail = S > 1 ? 4.9 : 1.6, fixed = 1.9;
+  // the K split's reduction moves BN columns of fp32 partials per row: its
+  // tail grows with the tile width (fit to the decode sweep: 64-wide tiles
+  // split 4 ways 10.7 us against 12.3-13.4 for 128-wide on 128x2112x7168)
+  const double head = 3.06, tail = S > 1 ? 1.6 + 3.3 * in.block_n / 128.0 : 1.6, fixed = 1.9;
   const double per_tile = 0.92 + (in.bs && in.nacc == 1 ? 0.4 : 0.0);
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);

@@ -1125,7 +1125,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
       }
     }  // tile loop
-    if (lane == 0) bulk_wait_group0();
+    // the staging tile must outlive the last stores' reads of it; their
+    // writes need no wait here (they are performed before the grid counts as
+    // complete, which is what a dependent launch and the host wait for)
+    if (lane == 0) bulk_wait_group_read0();
     cp_async_wait_all();   // (after an abort, scale copies may still be in flight)
     __syncwarp();
   }

@@ -655,7 +655,9 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
       }
     }
-    if (hlead) bulk_wait_group0();
+    // (the staging must outlive the last stores' reads; their writes are
+    // performed before the grid counts as complete)
+    if (hlead) bulk_wait_group_read0();
     __syncwarp();
   }
 

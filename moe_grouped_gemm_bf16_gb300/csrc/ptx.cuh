@@ -135,10 +135,6 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_group0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Makes generic-proxy writes to shared memory visible to the async proxy
 // (TMA store reads them).
 __device__ __forceinline__ void fence_proxy_async_smem() {
