@@ -392,6 +392,80 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+class NvmlSampler:
+    """Reads of SM clock, clock-event reasons and power through NVML (the
+    driver's libnvidia-ml, called with ctypes; reads only) every ~1 ms on a
+    thread, so that a timed region of a few tens of milliseconds still gets
+    tens of samples.  Same record as ClockSampler.summarize; None when NVML
+    cannot be loaded."""
+
+    # clock-event reason bits (nvml.h): SW power cap, HW slowdown, SW thermal, HW thermal
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, gpu_index, period_s=0.001):
+        self.gpu = gpu_index
+        self.period = period_s
+        self.samples = []          # (time, sm_mhz, reasons, power_mw)
+        self.run = False
+        self.thread = None
+        self.lib = None
+        self.dev = None
+        self.max_mhz = None
+
+    def start(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            dev = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(dev)) != 0:
+                return False
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(dev, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except Exception:
+            return False
+        self.lib, self.dev, self.ct = lib, dev, ctypes
+        self.run = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        return True
+
+    def _loop(self):
+        ct, lib, dev = self.ct, self.lib, self.dev
+        mhz, rs, mw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        while self.run:
+            ok = lib.nvmlDeviceGetClockInfo(dev, ct.c_int(1), ct.byref(mhz)) == 0  # NVML_CLOCK_SM
+            r = rs.value if self.reasons_fn(dev, ct.byref(rs)) == 0 else 0
+            p = mw.value if lib.nvmlDeviceGetPowerUsage(dev, ct.byref(mw)) == 0 else None
+            if ok:
+                self.samples.append((time.time(), float(mhz.value), r, p))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.run = False
+        if self.thread:
+            self.thread.join(timeout=2)
+        return self.samples
+
+    def summarize(self, t0=None, t1=None):
+        sel = [s for s in self.samples
+               if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        if not sel:
+            return None
+        reasons = sorted({nm for s in sel for nm, b in self.BITS.items() if s[2] & b})
+        pw = [s[3] / 1000.0 for s in sel if s[3] is not None]
+        return {"sm_mhz": statistics.median(s[1] for s in sel),
+                "sm_max_mhz": self.max_mhz or max(s[1] for s in sel),
+                "reasons": reasons, "samples": len(sel),
+                "power_w_max": round(max(pw), 1) if pw else None,
+                "source": f"NVML every {self.period * 1e3:.0f} ms"}
+
+
 # --------------------------------------------------------------- GPU arm ---
 class DeviceCase:
     """A case's tensors resident on the GPU and the library call on them."""
@@ -610,15 +684,32 @@ def run_ours(args):
     if sampler:
         sampler.start()
         sampler.wait_first()
-    spans = {}
+    nvml = NvmlSampler(local) if rank == 0 else None
+    if nvml and not nvml.start():
+        nvml = None
+    spans, exact = {}, {}
     for w in wls:
         a = time.time()
         w.ms = time_steps(w, torch, stream, steps, pg)
-        # (a region shorter than the sampling interval still gets its nearest samples)
-        spans[w.name] = (a - 0.06, time.time() + 0.06)
+        b = time.time()
+        exact[w.name] = (a, b)
+        # (a region shorter than nvidia-smi's interval still gets its nearest samples)
+        spans[w.name] = (a - 0.06, b + 0.06)
     if sampler:
         time.sleep(0.15)
     samples = sampler.stop() if sampler else None
+    if nvml:
+        nvml.stop()
+
+    def clocks_of(t0, t1, s0, s1):
+        """The clock record of a region: NVML's 1 ms reads inside it when
+        there are any, with nvidia-smi's samples around it beside them."""
+        smi = ClockSampler.summarize(samples, s0, s1) if samples else None
+        rec = nvml.summarize(t0, t1) if nvml else None
+        if rec is None:
+            return smi
+        rec["nvidia_smi"] = smi
+        return rec
     status = dg.get_device_status(stream.cuda_stream)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed regions")
@@ -637,7 +728,7 @@ def run_ours(args):
         rec["workload"] = w.describe(args)
         rec["l2"] = w.l2_note()
         if samples:
-            rec["clocks"] = ClockSampler.summarize(samples, *spans[w.name])
+            rec["clocks"] = clocks_of(*exact[w.name], *spans[w.name])
         detail[w.name] = rec
     for w in wls:
         if rank == 0 and not args.quick:
@@ -675,8 +766,8 @@ def run_ours(args):
         "e2e": h["e2e"],
         "gpu_launches": h["gpu_launches"],
         "gpu_launches_all_workloads": sum(detail[n]["gpu_launches"] for n in names),
-        "clocks": (ClockSampler.summarize(samples, spans[names[0]][0], spans[names[-1]][1])
-                   if samples else None),
+        "clocks": clocks_of(exact[names[0]][0], exact[names[-1]][1], spans[names[0]][0],
+                            spans[names[-1]][1]),
         "cases": h.get("per_case"),
     }
     if len(names) > 1:

@@ -109,3 +109,18 @@ def test_oracle_sample_shape_fits_the_budget():
     assert rows == 8 and cols % 16 == 0 and cols < 1024
     rows, cols = b._sample_shape(c, 1e6, 1e9, 8)
     assert rows == 4096 and cols == 1024
+
+
+def test_nvml_sampler_summary_reads_reason_bits():
+    """The NVML clock record: median SM clock of the reads inside the region,
+    the clock-event reasons from their bits, power in W."""
+    import bench
+    s = bench.NvmlSampler(0)
+    s.max_mhz = 2070.0
+    s.samples = [(1.0, 2070.0, 0, 900000), (2.0, 2000.0, 0x4, 1200000), (3.0, 1990.0, 0x4, 1300000),
+                 (9.0, 1000.0, 0x8 | 0x40, 100000)]
+    rec = s.summarize(0.5, 3.5)
+    assert rec["sm_mhz"] == 2000.0 and rec["samples"] == 3 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["power_w_max"] == 1300.0
+    assert s.summarize(8.5, 9.5)["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert s.summarize(20, 30) is None
