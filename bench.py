@@ -828,13 +828,18 @@ def run_e2e(dcs, cases, torch, stream, steps, pg, world, unit="GB/s"):
     h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
 
-    # Two streams: the inputs of case i+1 travel host -> device while case i
-    # computes and its result travels device -> host (the two directions of the
-    # link run concurrently; one direction alone is the bound).  A case's input
-    # buffers are refilled only after the previous step's kernel on them ended.
+    # Three streams, chained by events and never synchronised inside the timed
+    # region: inputs host -> device on s_in, the GEMMs on `stream`, results
+    # device -> host on s_out.  So the inputs of the next case (and of the next
+    # step) travel while a case computes and an earlier result travels back:
+    # the two directions of the link run at once.  A case's input buffers are
+    # refilled only after its previous kernel ended, and its output buffer is
+    # rewritten only after the previous read-back of it ended.
     s_in = torch.cuda.Stream()
+    s_out = torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in dcs]
     ev_done = [torch.cuda.Event() for _ in dcs]
+    ev_out = [torch.cuda.Event() for _ in dcs]
     started = [False]
 
     def one_step():
@@ -847,25 +852,36 @@ def run_e2e(dcs, cases, torch, stream, steps, pg, world, unit="GB/s"):
                 ev_in[i].record(s_in)
             with torch.cuda.stream(stream):
                 stream.wait_event(ev_in[i])
+                if started[0]:
+                    stream.wait_event(ev_out[i])
                 d.call(stream.cuda_stream)
                 ev_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[i])
                 ho.copy_(d.D, non_blocking=True)
+                ev_out[i].record(s_out)
         started[0] = True
-        stream.synchronize()
-        s_in.synchronize()
+
+    def sync_all():
+        for st in (s_in, stream, s_out):
+            st.synchronize()
 
     one_step()
+    sync_all()
     barrier(pg)
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
+    sync_all()
     dt = max_over_ranks(pg, time.perf_counter() - t0)
     per = dt / steps
     return {"value": round(world * value_of(cases, per, unit), 2), "unit": unit,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": round(per * 1e3, 4),
-            "copies": "pinned host buffers; inputs on a second stream, overlapping the "
-                      "previous case's kernel and result read-back"}
+            "copies": "pinned host buffers; inputs, kernels and read-backs on three streams "
+                      "chained by events (every step copies all its inputs in and all its "
+                      "outputs out; the next inputs travel while earlier results return), one "
+                      "synchronisation at the end of the timed steps"}
 
 
 # -------------------------------------------------------- CPU oracle arm ---
