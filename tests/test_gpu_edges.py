@@ -1,0 +1,85 @@
+"""Degenerate and extreme inputs of the grouped forms, through the C ABI,
+against the CPU oracle: every masked group empty, every contiguous block
+padding, the smallest shapes, and the largest group count the masked form
+takes (1024)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_bf16_gb300 as dg
+import oracle
+import workloads as W
+from moe_grouped_gemm_bf16_gb300 import _build
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+ORC = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    global ORC
+    _build.build()
+    ORC = oracle.Oracle()
+    torch.cuda.init()
+    yield
+    dg.debug_force_config(0, 0)
+    dg.debug_force_pair(-1)
+
+
+def _check_masked(p, mm, what):
+    got = U.run_masked(p, masked_m=mm, expected_m=max(1, int(mm.mean())))
+    assert dg.get_device_status() == 0, what
+    init = np.full(got.shape, W.BF16_SENTINEL, np.uint16)
+    want = ORC.grouped_masked(p["A"], p["sa"], p["B"], p["sb"], mm, init)
+    for g in range(p["G"]):
+        v = int(mm[g])
+        assert np.all(got[g, v:] == W.BF16_SENTINEL), f"{what}: group {g} rows past masked_m written"
+        U.assert_close(got[g, :v], want[g, :v], f"{what}: group {g}")
+
+
+@pytest.mark.parametrize("cfg", [(0, 0, -1), (128, 1, 0), (256, 1, 1)],
+                         ids=lambda c: f"bn{c[0]}_pair{c[2]}")
+def test_masked_all_groups_empty(cfg):
+    """No group has a row: no tile exists, D is left as it was."""
+    p = W.masked_problem(4, 256, 528, 1024, 64, seed=301)
+    mm = np.zeros(4, np.int32)
+    dg.get_device_status()
+    with U.forced_config(*cfg):
+        _check_masked(p, mm, f"all empty {cfg}")
+
+
+def test_contiguous_all_padding():
+    """Every 128-row block is padding (m_indices = -1): D is all +0."""
+    p = W.contiguous_problem(2, 272, 512, 1, 100, seed=303)
+    p = dict(p)
+    p["m_indices"] = np.full(p["M"], -1, np.int32)
+    dg.get_device_status()
+    got = U.run_contiguous(p)
+    assert dg.get_device_status() == 0
+    assert np.all(got == 0)
+
+
+def test_smallest_shapes():
+    """One K group, N = 16, one row: masked (G = 1, max_m = 1) and
+    contiguous (one expert of one valid row in a 128-row block)."""
+    p = W.masked_problem(1, 1, 16, 128, 1, seed=305)
+    _check_masked(p, np.array([1], np.int32), "masked 1x16x128")
+    q = W.contiguous_problem(1, 16, 128, 1, 1, seed=307)
+    got = U.run_contiguous(q)
+    assert dg.get_device_status() == 0
+    want = ORC.grouped_contiguous(q["A"], q["sa"], q["B"], q["sb"], q["m_indices"])
+    pad = q["m_indices"] < 0
+    assert np.all(got[pad] == 0)
+    U.assert_close(got[~pad], want[~pad], "contiguous 1 row")
+
+
+def test_masked_most_groups():
+    """1024 groups (the largest count), each with 0..16 rows: the device's
+    prefix of M blocks spans 32 warp passes."""
+    p = W.masked_problem(1024, 16, 32, 128, 8, seed=309, m_lo=0)
+    mm = p["masked_m"].copy()
+    assert (mm == 0).any() and (mm == 16).any()
+    dg.get_device_status()
+    _check_masked(p, mm, "1024 groups")
