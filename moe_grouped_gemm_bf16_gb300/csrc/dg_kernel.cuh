@@ -143,10 +143,12 @@ __device__ __forceinline__ void dbg_fail(const Params& p, unsigned int code,
 // owns rows [128 * crank, 128 * crank + 128).
 // K-grouped form: the tiles of group g come before those of g + 1 (each group
 // rasterised alone); `prefix` holds the groups' first K groups.
+// The contiguous form's expert id of the tile's first row is read from
+// m_indices unless the caller passes it (pre_e >= -1, fetched ahead).
 template <int BN, int MODE, bool PAIR = false>
 __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_blocks,
                                             const int* prefix, const int* mcnt, int kb0, int kb1,
-                                            uint32_t crank = 0) {
+                                            uint32_t crank = 0, int pre_e = -2) {
   const int nN = p.num_n_blocks;
   int kg = 0;
   if (MODE == kKGrouped) {
@@ -184,7 +186,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
   } else if (MODE == kContiguous) {
     T.m0 = mb * BLOCK_M;
     T.z = 0;
-    const int e = __ldg(p.m_indices + T.m0);
+    const int e = pre_e >= -1 ? pre_e : __ldg(p.m_indices + T.m0);
     T.e = e;
     T.rows = BLOCK_M;
     if (e < 0) {
@@ -212,6 +214,17 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, int num_m_bl
   }
   T.zd = T.z;
   return T;
+}
+
+// First row of tile t in the contiguous form (decode_tile's raster order),
+// so that its expert id can be fetched a tile ahead.
+__device__ __forceinline__ int contiguous_tile_m0(int t, const Params& p, int num_m_blocks) {
+  const int band_tiles = p.raster_m * p.num_n_blocks;
+  const int band = t / band_tiles;
+  const int r = t - band * band_tiles;
+  const int bm0 = band * p.raster_m;
+  const int bh = min(p.raster_m, num_m_blocks - bm0);
+  return (bm0 + r % bh) * BLOCK_M;
 }
 
 // Checked build: the coordinates of a tile's loads for K group g lie inside
@@ -788,8 +801,22 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       sb_issue(cluster_id, 0);
       cp_async_mbar_arrive_noinc(bar(L::SB_FULL + 0));
     }
+    // contiguous form: the expert id of the next tile's first row, and each
+    // row's id for this tile's epilogue, are loaded a tile / a main loop
+    // ahead (each load is a round trip to memory that would otherwise stall
+    // the promotion warps at the tile's start and at its epilogue)
+    int e_next = (MODE == kContiguous && cluster_id < num_tiles)
+                     ? __ldg(p.m_indices + contiguous_tile_m0(cluster_id, p, num_m_blocks))
+                     : -2;
     for (int t = cluster_id; t < num_tiles; t += tile_stride, ++k_iter) {
-      const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
+      const Tile T = decode_tile<BN, MODE, PAIR>(t, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank,
+                                                 MODE == kContiguous ? e_next : -2);
+      int row_id = -1;
+      if constexpr (MODE == kContiguous) {
+        if (!T.skip) row_id = __ldg(p.m_indices + T.m0 + row);
+        if (t + tile_stride < num_tiles)
+          e_next = __ldg(p.m_indices + contiguous_tile_m0(t + tile_stride, p, num_m_blocks));
+      }
       // Dense form with an addend (D = C + A B^T): thread 0 loads this tile's C
       // into the staging tile, in the store's own layout, halfway through the
       // tile's K groups (the previous tile's store has long finished reading
@@ -920,7 +947,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             zero_row = true;
             if (T.skip == 2 && pt == 0) raise_status(p, ST_EXPERT_RANGE);
           } else {
-            const int id = __ldg(p.m_indices + T.m0 + row);
+            const int id = row_id;
             if (id != T.e) {
               zero_row = true;
               if (id >= 0) raise_status(p, ST_EXPERT_RANGE);  // block mixes two experts
