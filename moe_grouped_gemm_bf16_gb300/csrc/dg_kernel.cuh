@@ -12,10 +12,12 @@
 //
 // Structure (one persistent CTA per SM, a CTA pair, or one cluster of split_k
 // CTAs per tile):
-//   warp 0      TMA producer: A tile [128 x 128], B tile [BN x 128] into an
+//   warps 0, 3  TMA producers (lane 0 of each, owning the ring slots of one
+//               parity): A tile [128 x 128], B tile [BN x 128] into an
 //               S-stage ring; the activation scales of four K groups at a
 //               time into a separate ring (they are read later, by the
-//               promotion warps).
+//               promotion warps); warp 0 also bulk-copies each tile's B
+//               scales into one of two buffers, a tile ahead.
 //   warps 1-2   warp 1 allocates tensor memory; the two warps take the K groups
 //               in turn, one thread each issuing 4 tcgen05.mma (K = 32 each)
 //               per K group into one of 2-4 TMEM accumulators, then
@@ -26,7 +28,8 @@
 //               registers while the tensor cores already compute the next
 //               group (the two-level accumulation of the pages: DeepSeek's
 //               overview deepep.org/zh/deepgemm, "细粒度缩放" / "核心优化技术").
-//               Then the bf16 epilogue: a swizzled staging tile stored by TMA,
+//               Then the bf16 epilogue: a swizzled staging tile stored by TMA
+//               (each promotion warp issuing some of the stores),
 //               or, when the K groups are split over a cluster, a fixed-order
 //               reduction of partials read through distributed shared memory.
 //
