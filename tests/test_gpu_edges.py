@@ -83,3 +83,41 @@ def test_masked_most_groups():
     assert (mm == 0).any() and (mm == 16).any()
     dg.get_device_status()
     _check_masked(p, mm, "1024 groups")
+
+
+def test_b_scales_not_16_byte_aligned():
+    """sb only 4-byte aligned (allowed by the ABI): the tile's B scales are
+    then fetched by the promotion threads instead of the producer's bulk
+    copies (which need 16-byte aligned rows); K/128 = 8 would otherwise take
+    the bulk path.  Dense and masked, against the oracle."""
+    p = W.dense_problem(200, 400, 1024, seed=311)
+    M, N, K = p["M"], p["N"], p["K"]
+    A, sa, B = U.dev(p["A"]), U.dev(p["sa"]), U.dev(p["B"])
+    sb_flat = np.concatenate([np.zeros(1, np.float32), p["sb"].ravel()])
+    sb_buf = U.dev(sb_flat)
+    sb = sb_buf[1:]                      # 4 bytes past a 16-byte boundary
+    assert sb.data_ptr() % 16 == 4
+    D = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    dg.get_device_status()
+    dg.gemm_fp8_fp8_bf16_nt(A, sa, sa.shape[-1], B, sb, D, M, N, K)
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    U.assert_close(U.to_bits(D), ORC.gemm_nt(p["A"], p["sa"], p["B"], p["sb"]), "dense, sb + 4 B")
+
+    q = W.masked_problem(3, 256, 400, 1024, 90, seed=313)
+    mm = q["masked_m"].copy()
+    A, sa, B = U.dev(q["A"]), U.dev(q["sa"]), U.dev(q["B"])
+    sb_buf = U.dev(np.concatenate([np.zeros(1, np.float32), q["sb"].ravel()]))
+    sb = sb_buf[1:]
+    D = torch.full((3, 256, 400), -1, dtype=torch.int16, device="cuda")
+    dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked(A, sa, sa.shape[-1], B, sb, D, U.dev(mm), 3, 256,
+                                             400, 1024, 90)
+    torch.cuda.synchronize()
+    assert dg.get_device_status() == 0
+    got = U.to_bits(D)
+    init = np.full(got.shape, 0xFFFF, np.uint16)
+    want = ORC.grouped_masked(q["A"], q["sa"], q["B"], q["sb"], mm, init)
+    for g in range(3):
+        v = int(mm[g])
+        assert np.all(got[g, v:] == 0xFFFF)
+        U.assert_close(got[g, :v], want[g, :v], f"masked, sb + 4 B, group {g}")
