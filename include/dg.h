@@ -305,9 +305,16 @@ typedef struct dg_config {
   int grid;         /* CTAs launched */
   int smem_bytes;   /* dynamic shared memory per CTA */
   int pair;         /* 1: CTA-pair form (a 2-CTA cluster computes each block_m = 256 tile) */
+  int block_scaled; /* 1: the block-scaled kernel (packed UE8M0 scales applied by the MMA) */
 } dg_config;
 dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
                          dg_config* out);
+
+/* The same for the "_ue8m0" entry points of each kind (packed UE8M0 scales),
+ * which choose between the block-scaled kernels and the promotion kernels'
+ * packed-scale twins (block_scaled says which). */
+dg_status dg_plan_config_ue8m0(int kind, int m, int n, int k, int num_groups, int num_sms,
+                               dg_config* out);
 
 /* Number of BLOCK_M x BLOCK_N output tiles of an M x N output (the unit of the
  * persistent scheduler; deepep.org/zh/deepgemm, "核心优化技术", unaligned block

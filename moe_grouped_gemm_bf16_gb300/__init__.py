@@ -53,7 +53,8 @@ EXPORTED_SYMBOLS = [
     "dg_m_grouped_gemm_fp8_fp8_bf16_nt_masked", "dg_quantize_fp8_1x128", "dg_get_num_sms",
     "dg_set_num_sms",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout",
-    "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_num_output_tiles",
+    "dg_last_error_string", "dg_get_device_status", "dg_plan_config", "dg_plan_config_ue8m0",
+    "dg_num_output_tiles",
     "dg_set_wait_timeout_ns", "dg_debug_set_skip_producer", "dg_debug_force_config",
     "dg_debug_force_pair", "dg_debug_force_block_scaled",
 ]
@@ -69,7 +70,7 @@ class DGError(RuntimeError):
 class DGConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("block_m", "block_n", "split_k", "stages", "num_tiles", "grid", "smem_bytes",
-                 "pair")]
+                 "pair", "block_scaled")]
 
 
 _LIB = None
@@ -118,6 +119,7 @@ def lib():
         L.dg_last_error_string.restype = ctypes.c_char_p
         L.dg_get_device_status.argtypes = [_vp]
         L.dg_plan_config.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(DGConfig)]
+        L.dg_plan_config_ue8m0.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(DGConfig)]
         L.dg_num_output_tiles.argtypes = [_i, _i, _i, _i]
         L.dg_num_output_tiles.restype = ctypes.c_longlong
         L.dg_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
@@ -291,10 +293,10 @@ def get_device_status(stream=None):
     return int(lib().dg_get_device_status(_stream(stream)))
 
 
-def plan_config(kind, m, n, k, num_groups=1, num_sms=152):
+def plan_config(kind, m, n, k, num_groups=1, num_sms=152, ue8m0=False):
     cfg = DGConfig()
-    _check(lib().dg_plan_config(int(kind), int(m), int(n), int(k), int(num_groups), int(num_sms),
-                                ctypes.byref(cfg)))
+    fn = lib().dg_plan_config_ue8m0 if ue8m0 else lib().dg_plan_config
+    _check(fn(int(kind), int(m), int(n), int(k), int(num_groups), int(num_sms), ctypes.byref(cfg)))
     return {f: getattr(cfg, f) for f, _ in DGConfig._fields_}
 
 

@@ -141,7 +141,7 @@ int smem_for(const Instance& in, int kb, int num_groups) {
   // the promotion kernels keep two tiles' B scales in shared memory (one
   // buffer filled while the other is read); the block-scaled ones read them
   // into the scale-factor staging instead
-  int s = in.fixed_smem + (in.bs ? 0 : 2 * 3 * kb * 4) +
+  int s = in.fixed_smem + (in.bs ? 0 : 2 * dgk::sb_buf_words(kb) * 4) +
           (in.mode == dgk::kMasked     ? (2 * num_groups + 1) * 4
            : in.mode == dgk::kKGrouped ? (num_groups + 1) * 4
                                        : 0);
@@ -167,8 +167,9 @@ struct Plan {
 //  * a CTA's K group costs the slowest of: the MMA/promotion cadence (0.22 us
 //    for 128-wide tiles, 0.50 us for 256-wide, 0.39 us for a CTA pair's
 //    256 x 256 tile), its share of HBM bandwidth for the B tile (~9 TB/s
-//    aggregate, L2 hits included), and the SM's TMA ingest for A and B
-//    (~100 GB/s per SM);
+//    aggregate, L2 hits included; a B tile is read from DRAM once by the M
+//    blocks of a raster band that share it), and the SM's TMA ingest for A
+//    and B (~100 GB/s per SM);
 //  * each wave of CTAs pays ~3 us before its first operands land and a tail
 //    (~4.9 us for the K split's cluster reduction, ~1.6 us otherwise);
 //  * a persistent CTA pays ~0.9 us per extra tile (epilogue), plus ~1.9 us per
@@ -177,21 +178,24 @@ struct Plan {
 // paying its own head and tail: this is what the model must steer away from.
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
-  (void)kind; (void)n; (void)num_groups;
-  // block-scaled: ~0.46 us per K group and CTA (per CTA pair for the pair
-  // form) for every tile width, one or two issuers (measured on the prefill
-  // and contiguous shapes: the TMA writes and the MMAs' operand reads share
+  (void)n;
+  // block-scaled: ~0.46 us per K group and CTA at 256 columns, 0.49 at 224
+  // (two accumulators), 0.44 at 128, 0.47 per K group of a CTA pair (measured
+  // on the prefill shapes: the TMA writes and the MMAs' operand reads share
   // the SM's shared-memory bandwidth); the MMA alone would take 0.13-0.27 us
-  const double t_cad = in.bs ? 0.46 : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
+  const double t_cad = in.bs ? (in.pair ? 0.47
+                                        : in.block_n <= 128 ? 0.44 : in.block_n == 224 ? 0.49 : 0.46)
+                             : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
   const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
-  // a block-scaled kernel with one accumulator waits for each tile's epilogue
-  // to read it before the next tile's MMAs
   // the K split's reduction moves BN columns of fp32 partials per row: its
   // tail grows with the tile width (fit to the decode sweep: 64-wide tiles
   // split 4 ways 10.7 us against 12.3-13.4 for 128-wide on 128x2112x7168)
   const double head = 3.06, tail = S > 1 ? 1.6 + 3.3 * in.block_n / 128.0 : 1.6, fixed = 1.9;
-  const double per_tile = 0.92 + (in.bs && in.nacc == 1 ? 0.4 : 0.0);
+  // (fitted: the block-scaled kernels with one accumulator wait for each
+  // tile's epilogue; the promotion kernels' packed-scale twins decode the
+  // scales of every K group, which weighs on short-K tiles)
+  const double per_tile = 0.92 + (in.bs && in.nacc == 1 ? 0.2 : 0.0) + (!in.bs && in.sfp ? 0.7 : 0.0);
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
   // the A box the TMA fills per K group (rows past M are zero-filled, not free)
@@ -213,7 +217,16 @@ double est_time_us(const Instance& in, int S, long long tiles, long long cluster
     ntile = cdiv(tiles, ctas);
     groups = ntile * kb;
   }
-  const double t_mem = b_rows * 128.0 / (bw_hbm / (double)ctas);
+  // B tiles come from DRAM once per raster band of M blocks that share them
+  // (dense; the M blocks of one expert in the contiguous form).  The masked
+  // form's few M blocks per group are taken as reading theirs each (fitted:
+  // the masked sweep's choices).
+  const long long bm = in.pair ? 256 : 128;
+  long long reuse = kind == dgk::kContiguous ? cdiv(m_rows, bm) / std::max(1, num_groups)
+                    : kind == dgk::kMasked   ? 1
+                                             : cdiv(m_rows, bm);
+  reuse = std::max(1LL, std::min<long long>(reuse, kRasterM));
+  const double t_mem = b_rows * 128.0 / (double)reuse / (bw_hbm / (double)ctas);
   const double t_tma = in.bs ? 0.0 : (a_rows + b_rows) * 128.0 / bw_sm;
   const double tg = std::max(t_cad, std::max(t_mem, t_tma));
   return fixed + (double)waves * (head + (double)groups * tg + tail) + (double)(ntile - 1) * per_tile;
@@ -247,12 +260,12 @@ Plan choose(int kind, long long m_rows, int n, int k, int num_groups, int num_sm
     const bool forced = force_bn > 0 || force_split > 0;
     if (in.a_rows < 128 && (m_rows > in.a_rows || !forced)) continue;
     // The CTA-pair form measured slower than the 128-row form on every shape
-    // so far (its promotion, not the MMA, sets the pace): it runs only when
-    // forced.
-    // (the block-scaled pair form is the heuristic's own choice)
+    // so far (the promotion kernels: their promotion, not the MMA, sets the
+    // pace; the block-scaled ones: 1-15% on the prefill shapes, up to 1.7x on
+    // the masked ones): it runs only when forced.
     const int fp = g_force_pair.load();
     if (fp == 0 && in.pair) continue;
-    if (fp < 0 && in.pair && !in.bs) continue;
+    if (fp < 0 && in.pair) continue;
     if (fp == 1 && !in.pair) continue;
     const int fbs = g_force_bs.load();
     if ((fbs == 0 && in.bs) || (fbs == 1 && !in.bs)) continue;
@@ -841,8 +854,9 @@ dg_status dg_get_device_status(void* stream) {
   }
 }
 
-dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
-                         dg_config* out) {
+namespace {
+dg_status plan_config(int kind, int m, int n, int k, int num_groups, int num_sms, bool sfp,
+                      dg_config* out) {
   read_env_once();
   if (!out || kind < 0 || kind > 3 || m < 1 || n < 16 || n % 16 || k < 128 || k % 128 ||
       k > 128 * dgk::MAX_KB || num_sms < 1 || (kind != dgk::kDense && num_groups < 1))
@@ -868,9 +882,9 @@ dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_
   };
   const int layout = kind == dgk::kKGrouped ? dgk::kTN : dgk::kNT;
   const Plan pl = choose(kind, m, n, k, G, num_sms, cap, g_force_bn.load(), g_force_split.load(),
-                         layout);
+                         layout, sfp);
   if (pl.inst < 0) return fail(DG_ERR_UNSUPPORTED_SHAPE, "no configuration");
-  const Instance& in = table_for(table_id(kind, layout)).p[pl.inst];
+  const Instance& in = table_for(table_id(kind, layout, sfp)).p[pl.inst];
   out->block_m = in.pair ? 2 * dgk::BLOCK_M : dgk::BLOCK_M;
   out->pair = in.pair;
   out->block_n = in.block_n;
@@ -879,7 +893,19 @@ dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_
   out->num_tiles = (int)pl.tiles;
   out->grid = std::max(1, pl.clusters) * (pl.pair ? 2 : pl.split);
   out->smem_bytes = pl.smem;
+  out->block_scaled = in.bs ? 1 : 0;
   return ok();
+}
+}  // namespace
+
+dg_status dg_plan_config(int kind, int m, int n, int k, int num_groups, int num_sms,
+                         dg_config* out) {
+  return plan_config(kind, m, n, k, num_groups, num_sms, false, out);
+}
+
+dg_status dg_plan_config_ue8m0(int kind, int m, int n, int k, int num_groups, int num_sms,
+                               dg_config* out) {
+  return plan_config(kind, m, n, k, num_groups, num_sms, true, out);
 }
 
 long long dg_num_output_tiles(int m, int n, int block_m, int block_n) {

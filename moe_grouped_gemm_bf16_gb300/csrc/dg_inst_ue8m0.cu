@@ -13,6 +13,8 @@ const Instance* instances_dense_ue8m0(int* count) {
       InstanceOf<256, 5, true, kDense, 64, false, kNT, true>::make(),
       InstanceOf<256, 4, false, kDense, 128, true, kNT, true>::make(),
       InstanceOf<128, 6, false, kDense, 128, true, kNT, true>::make(),
+      InstanceOf<64, 8, false, kDense, 128, false, kNT, true>::make(),
+      InstanceOf<64, 8, true, kDense, 128, false, kNT, true>::make(),
   };
   *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
   return table;
@@ -31,6 +33,7 @@ const Instance* instances_masked_ue8m0(int* count) {
   static const Instance table[] = {
       InstanceOf<128, 5, false, kMasked, 128, false, kNT, true>::make(),
       InstanceOf<256, 3, false, kMasked, 128, false, kNT, true>::make(),
+      InstanceOf<64, 8, false, kMasked, 128, false, kNT, true>::make(),
       InstanceOf<256, 4, false, kMasked, 128, true, kNT, true>::make(),
       InstanceOf<128, 6, false, kMasked, 128, true, kNT, true>::make(),
   };

@@ -97,7 +97,7 @@ struct SmemLayout {
 template <int BN, int STAGES, bool SPLIT, int AROWS = BLOCK_M, bool PAIR = false>
 __host__ __device__ constexpr int smem_bytes(int kb, int num_groups, int mode) {
   return 1024 /* alignment slack */ + SmemLayout<BN, STAGES, SPLIT, AROWS, PAIR>::DYN_OFF +
-         2 * 3 * kb * 4 +
+         2 * sb_buf_words(kb) * 4 +
          (mode == kMasked ? (2 * num_groups + 1) * 4 : mode == kKGrouped ? (num_groups + 1) * 4 : 0);
 }
 
@@ -330,9 +330,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8 * i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
   volatile uint32_t* abort_flag = misc + 1;
-  // B scales of a tile, two buffers of [3][kb] (one filled while the other is read)
+  // B scales of a tile, two buffers (one filled while the other is read)
   float* sb_s = reinterpret_cast<float*>(smem + L::DYN_OFF);
-  int* prefix = reinterpret_cast<int*>(sb_s + 6 * p.kb);
+  const int sbw = sb_buf_words(p.kb);
+  int* prefix = reinterpret_cast<int*>(sb_s + 2 * sbw);
   int* mcnt = prefix + p.num_groups + 1;
   const float* sa_ring = reinterpret_cast<const float*>(smem + L::SA_OFF);
   // checked build: fills of each operand-ring slot, then of each scale-ring slot
@@ -348,13 +349,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // this CTA's K groups: a slice of them in the split form, all of them otherwise
   // (the pair form's cluster rank names a half of the tile, not of K)
   const uint32_t krank = SPLIT ? crank : 0;
-  // A tile's B scales come either from the producer (one bulk copy per
-  // 128-column block: whole 16-byte aligned rows of fp32 scales, i.e. no K
-  // split, no K-grouped form, K/128 a multiple of 4) or, otherwise, from the
-  // promotion threads' own 4-byte copies.  Either way they land in one of two
-  // buffers while the previous tile is promoted.
-  const bool sb_bulk = !SPLIT && !SFP && MODE != kKGrouped && (p.kb & 3) == 0 &&
-                       (reinterpret_cast<uintptr_t>(p.sb) & 15) == 0;
+  // A tile's B scales come either from the producer or from the promotion
+  // threads' own 4-byte copies (the K split, whose CTAs take a slice of each
+  // row, and the K-grouped form, whose rows are per group).  The producer
+  // copies, in one bulk copy, the 16-byte aligned span of global memory that
+  // holds the rows of the tile's 128-column blocks (consecutive rows of the
+  // scale tensor); a row starts `sb_lead` words into the span.  Either way
+  // they land in one of two buffers while the previous tile is promoted.
+  const bool sb_bulk = !SPLIT && MODE != kKGrouped;
+  const int sb_row = SFP ? p.kbp : p.kb;   // words per row of the scale tensor
+  auto sb_first_row = [&](const Tile& U) {
+    return reinterpret_cast<const uint32_t*>(p.sb) +
+           (static_cast<size_t>(U.e) * p.nb + (U.n0 >> 7)) * sb_row;
+  };
   const int kbeg = static_cast<int>(static_cast<long long>(krank) * p.kb / S);
   const int kend = static_cast<int>(static_cast<long long>(krank + 1) * p.kb / S);
 
@@ -531,15 +538,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (T.skip) {
               mbar_arrive(bar(L::SB_FULL + sbb));
             } else {
-              const uint32_t row_bytes = static_cast<uint32_t>(p.kb) * 4u;
-              mbar_arrive_expect_tx(bar(L::SB_FULL + sbb), 3u * row_bytes);
-              const uint32_t dst = smem_u32(sb_s + sbb * 3 * p.kb);
-              for (int jb = 0; jb < 3; ++jb) {
-                const int nbk = min((T.n0 >> 7) + jb, p.nb - 1);
-                bulk_load_g2s(dst + jb * row_bytes,
-                              p.sb + (static_cast<size_t>(T.e) * p.nb + nbk) * p.kb, row_bytes,
-                              bar(L::SB_FULL + sbb));
-              }
+              // the rows of the blocks the tile's columns touch, within N (the
+              // buffer's rows past them are never read for a stored column);
+              // the span is widened to 16-byte boundaries, which never leaves
+              // the memory pages of the rows themselves
+              const int nrows = min(((T.n0 & 127) + BN - 1) / 128 + 1, p.nb - (T.n0 >> 7));
+              const uintptr_t a = reinterpret_cast<uintptr_t>(sb_first_row(T));
+              const uintptr_t a0 = a & ~static_cast<uintptr_t>(15);
+              const uintptr_t a1 = (a + static_cast<uintptr_t>(nrows) * sb_row * 4u + 15) &
+                                   ~static_cast<uintptr_t>(15);
+              const uint32_t bytes = static_cast<uint32_t>(a1 - a0);
+              mbar_arrive_expect_tx(bar(L::SB_FULL + sbb), bytes);
+              bulk_load_g2s(smem_u32(sb_s + sbb * sbw), reinterpret_cast<const void*>(a0), bytes,
+                            bar(L::SB_FULL + sbb));
             }
           }
           sb_eph ^= 1u << sbb;
@@ -784,7 +795,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const Tile U = decode_tile<BN, MODE, PAIR>(tt, p, num_m_blocks, prefix, mcnt, kbeg, kend, crank);
       if (!U.skip) {
         const int tku = U.kend - U.kbeg;
-        float* dst = sb_s + buf * 3 * p.kb;
+        float* dst = sb_s + buf * sbw;
         for (int i = pt; i < 3 * tku; i += 32 * NUM_PROMO_WARPS) {
           const int jb = i / tku, gg = i - jb * tku;
           const int nbk = min((U.n0 >> 7) + jb, p.nb - 1);
@@ -841,7 +852,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       // this tile's B scales (every promotion thread's copies have landed);
       // the other buffer, last read by the previous tile, which every thread
       // has finished, takes the next tile's
-      const float* sbt = sb_s + sbi * 3 * p.kb;
+      // (bulk form: the tile's first row starts a few words into the span)
+      const float* sbt =
+          sb_s + sbi * sbw +
+          ((sb_bulk && !T.skip) ? (reinterpret_cast<uintptr_t>(sb_first_row(T)) >> 2) & 3 : 0);
+      // words between the rows of consecutive 128-column blocks
+      const int rstride = sb_bulk ? sb_row : tk;
       wait_bar(bar(L::SB_FULL + sbi), (sbph >> sbi) & 1u, abort_flag, p);
       sbph ^= 1u << sbi;
       const bool sb_next = t + tile_stride < num_tiles;
@@ -890,7 +906,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                                BLOCK_M + row], g);
           else
             a_s = sa_ring[(j * SA_GROUPS + r) * BLOCK_M + row];
-          const float* sbg = sbt + (g - T.kbeg);
+          // bulk form, packed scales: one word per four K groups
+          const float* sbg = sbt + ((sb_bulk && SFP) ? (g >> 2) : (g - T.kbeg));
           const uint32_t tcol = t_lane + static_cast<uint32_t>(b * BN + h * HALF);
           // PROMO_LB 32-column chunks per load batch: tcgen05.wait::ld waits for
           // every outstanding load, so fewer, larger batches expose its latency
@@ -913,7 +930,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               const int c = bt * LB + u;
               const int col = h * HALF + c * 32;
               // the 32 columns lie in one 128-column B scale block
-              const float sb_v = sbg[((nmod + col) >> 7) * tk];
+              const float sb_v = sbg[((nmod + col) >> 7) * rstride];
               const float sc = a_s * (SFP ? ue8m0_scale(__float_as_uint(sb_v), g) : sb_v);
 #pragma unroll
               for (int i = 0; i < 32; i += 2)

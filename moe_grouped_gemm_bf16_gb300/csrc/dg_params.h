@@ -45,6 +45,12 @@ constexpr int MAX_GROUPS_MASKED = 1024;
 constexpr int MAX_GROUPS_KGROUPED = 1024;
 constexpr int MAX_KB = 512;   // K <= 65536
 constexpr int MAX_SPLIT = 8;  // CTAs per cluster in the K-split form
+// 32-bit words of one of a CTA's two B-scale buffers: a tile's [3][K/128]
+// scales (per K group), or the 16-byte aligned span of global memory holding
+// the rows of its (up to 3) 128-column blocks (fp32: K/128 words per row,
+// packed UE8M0: K/512), which starts up to 3 words before the first row and
+// ends up to 3 words after the last.
+__host__ __device__ constexpr int sb_buf_words(int kb) { return (3 * kb + 8 + 3) & ~3; }
 
 // Checked build (compiled with -DDG_DEBUG=1; the library libdg_debug.so):
 // before every TMA load and every plain global store the kernels check the

@@ -265,6 +265,18 @@ def test_plan_config_heuristic(L):
         dg.plan_config(0, 64, 2112, 7000, 1, 152)
     with pytest.raises(dg.DGError):
         dg.plan_config(4, 64, 2112, 7168, 1, 152)
+    with pytest.raises(dg.DGError):
+        dg.plan_config(4, 64, 2112, 7168, 1, 152, ue8m0=True)
+    # the fp32-scale entry points have no block-scaled kernel
+    for kind, m, g in ((0, 4096, 1), (1, 32768, 4), (2, 256, 8), (0, 64, 1)):
+        assert dg.plan_config(kind, m, 7168, 7168, g, 152)["block_scaled"] == 0
+    # packed UE8M0 scales: the block-scaled kernel for prefill and the grouped
+    # prefill shapes; decode keeps the promotion kernels' K split
+    for kind, m, g in ((0, 4096, 1), (1, 32768, 4), (2, 256, 8)):
+        cfg = dg.plan_config(kind, m, 7168, 7168, g, 152, ue8m0=True)
+        assert cfg["block_scaled"] == 1 and cfg["split_k"] == 1, (kind, cfg)
+    cfg = dg.plan_config(0, 64, 7168, 7168, 1, 152, ue8m0=True)
+    assert cfg["block_scaled"] == 0 and cfg["split_k"] > 1
 
 
 def test_force_config_hook(L):

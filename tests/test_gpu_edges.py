@@ -86,10 +86,10 @@ def test_masked_most_groups():
 
 
 def test_b_scales_not_16_byte_aligned():
-    """sb only 4-byte aligned (allowed by the ABI): the tile's B scales are
-    then fetched by the promotion threads instead of the producer's bulk
-    copies (which need 16-byte aligned rows); K/128 = 8 would otherwise take
-    the bulk path.  Dense and masked, against the oracle."""
+    """sb only 4-byte aligned (allowed by the ABI): the producer's bulk copy of
+    a tile's B-scale rows then starts up to 12 bytes before the first row (the
+    16-byte boundary below it) and the promotion reads from that offset.
+    Dense and masked, against the oracle."""
     p = W.dense_problem(200, 400, 1024, seed=311)
     M, N, K = p["M"], p["N"], p["K"]
     A, sa, B = U.dev(p["A"]), U.dev(p["sa"]), U.dev(p["B"])
@@ -121,3 +121,67 @@ def test_b_scales_not_16_byte_aligned():
         v = int(mm[g])
         assert np.all(got[g, v:] == 0xFFFF)
         U.assert_close(got[g, :v], want[g, :v], f"masked, sb + 4 B, group {g}")
+
+
+@pytest.mark.parametrize("K", [640, 1152, 2560], ids=lambda k: f"K{k}")
+def test_packed_b_scales_not_16_byte_aligned(K):
+    """Packed UE8M0 B scales (K/512 words per row, rounded up) 4 bytes past a
+    16-byte boundary, through the promotion kernels' packed-scale twins (the
+    block-scaled kernels switched off): rows of 2, 3 and 5 words, so the tiles'
+    spans start at every offset within a 16-byte unit.  Dense and masked."""
+    kb, kbp = K // 128, (K // 128 + 3) // 4
+    p = W.dense_problem(200, 656, K, seed=315 + K)
+    M, N = p["M"], p["N"]
+    nb = (N + 127) // 128
+    g = torch.Generator().manual_seed(K)
+    e_a = torch.randint(120, 134, (M, kb), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+    e_b = torch.randint(120, 134, (nb, kb), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+
+    def pack(e):
+        pad = (-e.shape[-1]) % 4
+        e = np.concatenate([e, np.zeros(e.shape[:-1] + (pad,), np.uint8)], axis=-1)
+        return np.ascontiguousarray(e).view("<i4")
+
+    ld = W.tma_aligned_ld(M)
+    sfa = np.zeros((kbp, ld), np.int32)
+    sfa[:, :M] = pack(e_a).T
+    sfb = pack(e_b)                                   # [nb, kbp]
+    sb_buf = U.dev(np.concatenate([np.zeros(1, np.int32), sfb.ravel()]))
+    sb = sb_buf[1:]
+    assert sb.data_ptr() % 16 == 4
+    A, B = U.dev(p["A"]), U.dev(p["B"])
+    D = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    dg.debug_force_block_scaled(0)
+    try:
+        dg.get_device_status()
+        dg.gemm_fp8_fp8_bf16_nt_ue8m0(A, U.dev(sfa), ld, B, sb, D, M, N, K)
+        torch.cuda.synchronize()
+        assert dg.get_device_status() == 0
+        want = ORC.gemm_nt(p["A"], ORC.decode_sfa(sfa, kb), p["B"], ORC.decode_sfb(sfb, kb))
+        U.assert_close(U.to_bits(D), want[:M], f"dense ue8m0, sb + 4 B, K={K}")
+
+        q = W.masked_problem(3, 256, 400, K, 90, seed=317 + K)
+        G, mm = 3, q["masked_m"].copy()
+        nbq = (400 + 127) // 128
+        e_bq = torch.randint(120, 134, (G, nbq, kb), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+        e_aq = torch.randint(120, 134, (G, 256, kb), generator=g, dtype=torch.int32).to(torch.uint8).numpy()
+        ldq = q["sa"].shape[-1]
+        sfaq = np.zeros((G, kbp, ldq), np.int32)
+        sfaq[:, :, :256] = np.swapaxes(pack(e_aq), -1, -2)
+        sfbq = pack(e_bq)                             # [G, nbq, kbp]
+        sbq = U.dev(np.concatenate([np.zeros(1, np.int32), sfbq.ravel()]))[1:]
+        D = torch.full((G, 256, 400), -1, dtype=torch.int16, device="cuda")
+        dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(U.dev(q["A"]), U.dev(sfaq), ldq, U.dev(q["B"]),
+                                                       sbq, D, U.dev(mm), G, 256, 400, K, 90)
+        torch.cuda.synchronize()
+        assert dg.get_device_status() == 0
+        got = U.to_bits(D)
+        init = np.full(got.shape, 0xFFFF, np.uint16)
+        want = ORC.grouped_masked(q["A"], ORC.decode_sfa(sfaq, kb), q["B"], ORC.decode_sfb(sfbq, kb),
+                                  mm, init)
+        for z in range(G):
+            v = int(mm[z])
+            assert np.all(got[z, v:] == 0xFFFF)
+            U.assert_close(got[z, :v], want[z, :v], f"masked ue8m0, sb + 4 B, K={K}, group {z}")
+    finally:
+        dg.debug_force_block_scaled(-1)

@@ -71,7 +71,7 @@ def run_dense(p):
 
 SHAPES = [(64, 256, 640), (128, 2112, 1152), (200, 400, 2048), (333, 528, 896), (1024, 4096, 7168)]
 CFGS = [(0, 0, -1), (128, 1, 0), (256, 1, 0), (128, 3, 0), (128, 5, 0), (256, 3, 0), (128, 7, 0),
-        (256, 1, 1), (128, 1, 1)]
+        (256, 1, 1), (128, 1, 1), (64, 1, 0), (64, 4, 0)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -100,16 +100,18 @@ def test_same_scales_same_bits(cfg):
     assert np.array_equal(got, ref)
 
 
-def test_contiguous_ue8m0():
+@pytest.mark.parametrize("cfg", [(0, 0), (128, 0), (256, 0)], ids=lambda c: f"bn{c[0]}")
+def test_contiguous_ue8m0(cfg):
     q = W.contiguous_problem(3, 400, 1152, 100, 300, seed=8)
     G, K, N = q["G"], q["K"], q["N"]
     kb, ld = K // 128, q["sa"].shape[-1]
     sfa, sfb = _sfa(kb, ld, 9), _sfb((N + 127) // 128, kb, 10, lead=(G,))
     A, B = U.dev(q["A"]), U.dev(q["B"])
     D = torch.full((q["M"], N), -1, dtype=torch.int16, device="cuda")
-    dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(A, U.dev(sfa), ld, B, U.dev(sfb), D,
-                                                       U.dev(q["m_indices"]), q["M"], N, K, G)
-    torch.cuda.synchronize()
+    with U.forced_config(*cfg):
+        dg.m_grouped_gemm_fp8_fp8_bf16_nt_contiguous_ue8m0(A, U.dev(sfa), ld, B, U.dev(sfb), D,
+                                                           U.dev(q["m_indices"]), q["M"], N, K, G)
+        torch.cuda.synchronize()
     assert dg.get_device_status() == 0
     want = ORC.grouped_contiguous(q["A"], ORC.decode_sfa(sfa, kb), q["B"],
                                   ORC.decode_sfb(sfb, kb), q["m_indices"])
@@ -119,17 +121,19 @@ def test_contiguous_ue8m0():
     U.assert_close(got[~pad], want[~pad], "contiguous ue8m0")
 
 
-def test_masked_ue8m0():
+@pytest.mark.parametrize("cfg", [(0, 0), (64, 0), (128, 0), (256, 0)], ids=lambda c: f"bn{c[0]}")
+def test_masked_ue8m0(cfg):
     q = W.masked_problem(4, 256, 528, 1152, 90, seed=12)
     G, K, N, max_m = q["G"], q["K"], q["N"], q["max_m"]
     kb, ld = K // 128, q["sa"].shape[-1]
     sfa, sfb = _sfa(kb, ld, 13, lead=(G,)), _sfb((N + 127) // 128, kb, 14, lead=(G,))
     fill = np.uint16(U.W.BF16_SENTINEL).view(np.int16)
     D = torch.full((G, max_m, N), int(fill), dtype=torch.int16, device="cuda")
-    dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(U.dev(q["A"]), U.dev(sfa), ld, U.dev(q["B"]),
-                                                   U.dev(sfb), D, U.dev(q["masked_m"]), G, max_m,
-                                                   N, K, 90)
-    torch.cuda.synchronize()
+    with U.forced_config(*cfg, pair=0 if cfg[0] else -1):
+        dg.m_grouped_gemm_fp8_fp8_bf16_nt_masked_ue8m0(U.dev(q["A"]), U.dev(sfa), ld, U.dev(q["B"]),
+                                                       U.dev(sfb), D, U.dev(q["masked_m"]), G,
+                                                       max_m, N, K, 90)
+        torch.cuda.synchronize()
     assert dg.get_device_status() == 0
     init = np.full((G, max_m, N), U.W.BF16_SENTINEL, np.uint16)
     want = ORC.grouped_masked(q["A"], ORC.decode_sfa(sfa, kb), q["B"], ORC.decode_sfb(sfb, kb),
