@@ -451,17 +451,6 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t smem_addr, uint32_t ran
   return r;
 }
 
-// Bulk copy from this CTA's shared memory into another CTA's (addresses from
-// mapa), counted in bytes on that CTA's mbarrier.  Addresses and size: 16-byte
-// multiples.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                     uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
-      : "memory");
-}
-
 // Bulk copy global -> this CTA's shared memory, counted in bytes on `bar`.
 // Addresses and size: 16-byte multiples.
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
