@@ -78,8 +78,9 @@ struct BsLayout {
   static constexpr int BAR_OFF = SFS_OFF + BS_SFS * SFS_BYTES;
   static constexpr int FULL = 0, EMPTY = STAGES, SFS_FULL = 2 * STAGES,
                        SFS_EMPTY = SFS_FULL + BS_SFS, SFT_EMPTY = SFS_EMPTY + BS_SFS,
-                       T_FULL = SFT_EMPTY + BS_SFT, T_EMPTY = T_FULL + NACC,
-                       MMA_DONE = T_EMPTY + NACC, NUM_BARS = MMA_DONE + 1;
+                       SFT_FULL = SFT_EMPTY + BS_SFT, T_FULL = SFT_FULL + BS_SFT,
+                       T_EMPTY = T_FULL + NACC, MMA_DONE = T_EMPTY + NACC, SF_DONE = MMA_DONE + 1,
+                       NUM_BARS = SF_DONE + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // [0] TMEM base, [1] abort flag
   // checked build: fill counters of the operand ring's and the staging ring's slots
   static constexpr int DBG_OFF = MISC_OFF + 16;
@@ -155,9 +156,13 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     for (int k = 0; k < BS_SFS; ++k) {
       mbar_init(bar(L::SFS_FULL + k), PAIR ? 2 : 1);   // pair: both CTAs' preparations
-      mbar_init(bar(L::SFS_EMPTY + k), ISS);           // every issuer's copies
+      mbar_init(bar(L::SFS_EMPTY + k), 1);             // the slot's copies have read it
     }
-    for (int t = 0; t < BS_SFT; ++t) mbar_init(bar(L::SFT_EMPTY + t), 1);
+    for (int t = 0; t < BS_SFT; ++t) {
+      mbar_init(bar(L::SFT_EMPTY + t), 1);
+      mbar_init(bar(L::SFT_FULL + t), 1);
+    }
+    mbar_init(bar(L::SF_DONE), 1);
     for (int b = 0; b < NACC; ++b) {
       mbar_init(bar(L::T_FULL + b), ISS);
       mbar_init(bar(L::T_EMPTY + b), PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
@@ -351,47 +356,23 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int nw = PAIR ? BN : min(BN, (p.N - T.n0 + 15) & ~15);
         const uint32_t idesc0 = idesc_mxf8f6f4(PAIR ? 2 * BLOCK_M : BLOCK_M, nw, A_MN, B_MN, 0, 0);
         const uint32_t d0 = tmem_base + static_cast<uint32_t>((b * ISS + e) * BN);
-        int k = 0, tt = 0;
+        int tt = 0;
         uint32_t sfa = 0;
         uint32_t acc = 0;         // this accumulator's first MMA of the tile starts it
         for (int g = T.kbeg; g < T.kend; ++g, ++q) {
           const bool mine = ISS == 1 || ((g - T.kbeg) & 1) == e;
           if (g == T.kbeg || (g & 3) == 0) {
-            // a new packed word: its prepared scale factors into this issuer's
-            // tensor-memory slot (if it has a K group in the word)
-            const int wend = min(T.kend, (g & ~3) + 4);
-            const bool has = ISS == 1 || mine || wend - g >= 2;
-            k = static_cast<int>(u % BS_SFS);
+            // a new packed word: the scale-factor warp has copied its scale
+            // factors into this issuer's tensor-memory slot
             tt = static_cast<int>(u % L::SFT_PER);
             sfa = sf_col(e, tt);
-            if (u >= L::SFT_PER)   // the slot's previous MMAs have completed
-              wait_bar(bar(L::SFT_EMPTY + e * L::SFT_PER + tt), ((u / L::SFT_PER) - 1) & 1u,
-                       abort_flag, p);
-            bool ok_s = PAIR ? wait_bar<true>(bar(L::SFS_FULL + k), (u / BS_SFS) & 1u,
-                                              abort_flag, p)
-                             : wait_bar(bar(L::SFS_FULL + k), (u / BS_SFS) & 1u, abort_flag, p);
+            const bool ok_s = wait_bar(bar(L::SFT_FULL + e * L::SFT_PER + tt),
+                                       (u / L::SFT_PER) & 1u, abort_flag, p);
             tc_fence_after();
             if constexpr (kDebug) {
-              if (ok_s && dbg_sfs_fill[k] != u / BS_SFS + 1) {
+              // the word's staging has been filled (at least) u / BS_SFS + 1 times
+              if (ok_s && dbg_sfs_fill[u % BS_SFS] < u / BS_SFS + 1)
                 dbg_fail(p, ST_DEBUG_PHASE, abort_flag);
-                ok_s = false;
-              }
-            }
-            if (has && ok_s && ok_t) {
-              const uint32_t src = sbase + L::SFS_OFF + k * L::SFS_BYTES;
-              if constexpr (PAIR) {
-                tmem_cp_128x128b_pair(sfa, smem_desc_rows16(src, 128));
-#pragma unroll
-                for (int j = 0; j < (BN / 32 + 3) / 4; ++j)
-                  tmem_cp_32x128b_warpx4_pair(
-                      sfa + 4 + 4 * j, smem_desc_rows16(src + L::SFA_BYTES + j * L::SFB_BYTES, 128));
-              } else {
-                tmem_cp_128x128b(sfa, smem_desc_rows16(src, 128));
-#pragma unroll
-                for (int j = 0; j < (BN / 32 + 3) / 4; ++j)
-                  tmem_cp_32x128b_warpx4(
-                      sfa + 4 + 4 * j, smem_desc_rows16(src + L::SFA_BYTES + j * L::SFB_BYTES, 128));
-              }
             }
           }
           if (mine) {
@@ -426,14 +407,9 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             else mma_commit(bar(L::EMPTY + s));
           }
           if (g == T.kend - 1 || (g & 3) == 3) {
-            // the word's last group: its staging slot and tensor-memory slot free up
-            if constexpr (PAIR) {
-              mma_commit_pair_multicast(bar(L::SFS_EMPTY + k), 0x3);
-              mma_commit_pair_multicast(bar(L::SFT_EMPTY + e * L::SFT_PER + tt), 0x1);
-            } else {
-              mma_commit(bar(L::SFS_EMPTY + k));
-              mma_commit(bar(L::SFT_EMPTY + e * L::SFT_PER + tt));
-            }
+            // the word's last group: its tensor-memory slot frees up once these MMAs complete
+            if constexpr (PAIR) mma_commit_pair_multicast(bar(L::SFT_EMPTY + e * L::SFT_PER + tt), 0x1);
+            else mma_commit(bar(L::SFT_EMPTY + e * L::SFT_PER + tt));
             ++u;
           }
           if (++s == STAGES) { s = 0; ph ^= 1; }
@@ -455,6 +431,12 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // columns 0-3, by tcgen05.cp 128x128b), and for the tile's 32-column
     // chunk k the word of its B block into cell k % 4 of every row of copy
     // k / 4 (copied to every lane quarter, column 4 + k, by 32x128b.warpx4).
+    // Lane 0 then issues those copies itself, into the tensor-memory slot of
+    // each issuer with a K group in the word, once the slot's previous MMAs
+    // have completed, and commits them to the issuers' barriers: the issuer
+    // only waits for one barrier per word (its thread stalls on every
+    // instruction between its MMAs).  Pair form: the leader's lane 0 copies
+    // both CTAs' staging (cta_group::2) once both are filled.
     const uint32_t* sfa = reinterpret_cast<const uint32_t*>(p.sa_packed);
     const uint32_t* sfb = reinterpret_cast<const uint32_t*>(p.sb);
     uint32_t u = 0;
@@ -495,10 +477,55 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           if (lane == 0) dbg_sfs_fill[k] = dbg_sfs_fill[k] + 1;
         }
         if (lane == 0) {
-          if (PAIR && !leader) mbar_arrive_remote_release(bar(L::SFS_FULL + k), 0);
-          else mbar_arrive(bar(L::SFS_FULL + k));
+          if (PAIR && !leader) {
+            mbar_arrive_remote_release(bar(L::SFS_FULL + k), 0);
+          } else {
+            bool ok = true;
+            if constexpr (PAIR) {
+              mbar_arrive(bar(L::SFS_FULL + k));
+              ok = wait_bar<true>(bar(L::SFS_FULL + k), (u / BS_SFS) & 1u, abort_flag, p);
+            }
+            const int tt = static_cast<int>(u % L::SFT_PER);
+            // the issuers with a K group in this word (two issuers: by parity)
+            const int g0 = max(T.kbeg, w0 * 4), g1 = min(T.kend, w0 * 4 + 4);
+            for (int e = 0; e < ISS; ++e) {
+              const bool has = ISS == 1 || g1 - g0 >= 2 || ((g0 - T.kbeg) & 1) == e;
+              if (u >= L::SFT_PER)   // the slot's previous MMAs have completed
+                ok = wait_bar(bar(L::SFT_EMPTY + e * L::SFT_PER + tt), ((u / L::SFT_PER) - 1) & 1u,
+                              abort_flag, p) && ok;
+              tc_fence_after();
+              if (has && ok) {
+                const uint32_t tsf = sf_col(e, tt);
+                if constexpr (PAIR) {
+                  tmem_cp_128x128b_pair(tsf, smem_desc_rows16(dst, 128));
+#pragma unroll
+                  for (int j = 0; j < (BN / 32 + 3) / 4; ++j)
+                    tmem_cp_32x128b_warpx4_pair(
+                        tsf + 4 + 4 * j, smem_desc_rows16(dst + L::SFA_BYTES + j * L::SFB_BYTES, 128));
+                } else {
+                  tmem_cp_128x128b(tsf, smem_desc_rows16(dst, 128));
+#pragma unroll
+                  for (int j = 0; j < (BN / 32 + 3) / 4; ++j)
+                    tmem_cp_32x128b_warpx4(
+                        tsf + 4 + 4 * j, smem_desc_rows16(dst + L::SFA_BYTES + j * L::SFB_BYTES, 128));
+                }
+              }
+              // (every word completes a phase of every issuer's slot barrier)
+              if constexpr (PAIR) mma_commit_pair_multicast(bar(L::SFT_FULL + e * L::SFT_PER + tt), 0x1);
+              else mma_commit(bar(L::SFT_FULL + e * L::SFT_PER + tt));
+            }
+            // the staging slot is free once the copies have read it (pair: in both CTAs)
+            if constexpr (PAIR) mma_commit_pair_multicast(bar(L::SFS_EMPTY + k), 0x3);
+            else mma_commit(bar(L::SFS_EMPTY + k));
+          }
         }
       }
+    }
+    if (lane == 0 && (!PAIR || leader)) {
+      // the last copies have completed before the tensor memory is freed
+      if constexpr (PAIR) mma_commit_pair_multicast(bar(L::SF_DONE), 0x1);
+      else mma_commit(bar(L::SF_DONE));
+      drain_wait(bar(L::SF_DONE), 0, p);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
