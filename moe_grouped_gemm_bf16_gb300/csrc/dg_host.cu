@@ -179,23 +179,29 @@ struct Plan {
 double est_time_us(const Instance& in, int S, long long tiles, long long clusters_resident,
                    int num_sms, int kind, long long m_rows, int n, int k, int num_groups) {
   (void)n;
-  // block-scaled: ~0.46 us per K group and CTA at 256 columns, 0.49 at 224
-  // (two accumulators), 0.44 at 128, 0.47 per K group of a CTA pair (measured
-  // on the prefill shapes: the TMA writes and the MMAs' operand reads share
-  // the SM's shared-memory bandwidth); the MMA alone would take 0.13-0.27 us
-  const double t_cad = in.bs ? (in.pair ? 0.47
-                                        : in.block_n <= 128 ? 0.44 : in.block_n == 224 ? 0.49 : 0.46)
-                             : in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50);
+  // block-scaled: ~0.39 us per K group and CTA at 256 columns, 0.38 at 224
+  // (two accumulators), 0.375 at 128, 0.41 per K group of a CTA pair (fitted
+  // to every width on the prefill, contiguous and masked sweeps: the TMA
+  // writes and the MMAs' operand reads share the SM's shared-memory
+  // bandwidth); the MMA alone would take 0.13-0.27 us
+  // (the promotion kernels' packed-scale twins: ~18% slower per K group than
+  // with fp32 scales, measured on the prefill shapes)
+  const double t_cad = in.bs ? (in.pair ? 0.41
+                                        : in.block_n <= 128 ? 0.375 : in.block_n == 224 ? 0.38 : 0.387)
+                             : (in.pair ? 0.39 : (in.block_n <= 128 ? 0.22 : 0.50)) *
+                                   (in.sfp ? 1.18 : 1.0);
   const double bw_hbm = 9.0e6;   // bytes / us, whole GPU
   const double bw_sm = 102e3;    // bytes / us, one SM's TMA ingest
   // the K split's reduction moves BN columns of fp32 partials per row: its
   // tail grows with the tile width (fit to the decode sweep: 64-wide tiles
   // split 4 ways 10.7 us against 12.3-13.4 for 128-wide on 128x2112x7168)
   const double head = 3.06, tail = S > 1 ? 1.6 + 3.3 * in.block_n / 128.0 : 1.6, fixed = 1.9;
-  // (fitted: the block-scaled kernels with one accumulator wait for each
-  // tile's epilogue; the promotion kernels' packed-scale twins decode the
-  // scales of every K group, which weighs on short-K tiles)
-  const double per_tile = 0.92 + (in.bs && in.nacc == 1 ? 0.2 : 0.0) + (!in.bs && in.sfp ? 0.7 : 0.0);
+  // (fitted: a block-scaled kernel with one accumulator waits for each
+  // tile's epilogue, ~0.9 us more per tile, with two ~0.2 us; the promotion
+  // kernels' packed-scale twins decode the scales of every K group, which
+  // weighs on short-K tiles)
+  const double per_tile = 0.92 + (in.bs ? (in.nacc == 1 ? 0.9 : 0.18) : 0.0) +
+                          (!in.bs && in.sfp ? 0.7 : 0.0);
   const long long kb = k / 128;
   const long long kper = cdiv(kb, S);
   // the A box the TMA fills per K group (rows past M are zero-filled, not free)
