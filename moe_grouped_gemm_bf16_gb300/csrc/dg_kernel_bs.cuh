@@ -19,21 +19,26 @@
 //               K-grouped set-up (device prefix sums).
 //   warp 1      allocates tensor memory; lane 0 is an MMA issuer.
 //   warp 3      lane 0 is the second MMA issuer when ISS = 2.
-//               An issuer copies, per packed word (four K groups), the
-//               prepared scale factors into its tensor-memory slot, then per
-//               K group issues four block-scaled MMAs (K = 32 each) over the
-//               whole tile width, committing the stage back to the producers
-//               and, after the tile's last group, its accumulator to the
-//               epilogue.  With two issuers each takes every other K group of
-//               a tile into an accumulator of its own (the thread that issues
-//               tcgen05.mma stalls until the pipe takes it, and one thread's
-//               loop per K group outlasts the MMAs of a 224- or 256-wide
-//               tile); the epilogue adds the two.
+//               An issuer waits, per packed word (four K groups), for the
+//               word's scale factors in its tensor-memory slot, then per K
+//               group issues four block-scaled MMAs (K = 32 each) over the
+//               whole tile width, committing the stage back to the producers,
+//               the slot back to the scale-factor warp after the word's last
+//               group and, after the tile's last group, its accumulator to
+//               the epilogue.  With two issuers each takes every other K group
+//               of a tile into an accumulator of its own (the thread that
+//               issues tcgen05.mma stalls until the pipe takes it, and one
+//               thread's loop per K group outlasts the MMAs of a 224- or
+//               256-wide tile); the epilogue adds the two.
 //   warps 4-11  epilogue: tensor memory -> (+ C) -> bf16 -> swizzled staging
 //               buffer -> TMA store (masked tail tiles: row-guarded stores).
-//   warp 12     scale-factor preparation: reads the packed words of the
-//               tile's rows and B blocks from global memory and lays them out
-//               in shared memory as the tensor-memory copies expect.
+//   warp 12     scale factors: reads the packed words of the tile's rows
+//               and B blocks from global memory, lays them out in shared
+//               memory as the tensor-memory copies expect, and (lane 0) copies
+//               them into each issuer's slot with tcgen05.cp once the slot's
+//               previous MMAs have completed, committing the copies to the
+//               issuer's barrier (so an issuer waits on one barrier per word
+//               and issues nothing but MMAs and commits).
 //
 // Where the MMA reads its scale factors (measured on GB300 with distinct
 // codes in every tensor-memory cell): the scale of A's row m from lane m,
