@@ -592,9 +592,39 @@ fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       tc_fence_after();
 #pragma unroll
       for (int i = 0; i < NCH0; ++i) {
-        if (i < nch) {
-          // the chunk in two 16-column halves (registers: the second
-          // accumulator's half rides along)
+        if (ISS == 1 && i < nch) {
+          // one accumulator: the whole 32-column chunk per load (each wait
+          // for a tensor-memory load exposes its latency, and the next tile's
+          // MMAs wait for the last of them)
+          uint32_t v[32];
+          if (acc_in) {
+            tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b * BN + (c_lo + i) * 32), v);
+            tmem_wait_ld(v);
+          } else {
+#pragma unroll
+            for (int e2 = 0; e2 < 32; ++e2) v[e2] = 0u;
+          }
+          if (i == nch - 1 && !T.skip) {
+            // every tensor-memory load of this warp has completed: hand the
+            // accumulator back (pair: on the leader's barrier)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (PAIR && !leader) mbar_arrive_remote_relaxed(bar(L::T_EMPTY + b), 0);
+              else mbar_arrive(bar(L::T_EMPTY + b));
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            // D = C + A B: the addend added in fp32, then one rounding
+            const uint32_t cw = pk[i][e];
+            const float lo = __uint_as_float(v[2 * e]) + __uint_as_float(cw << 16);
+            const float hi = __uint_as_float(v[2 * e + 1]) + __uint_as_float(cw & 0xFFFF0000u);
+            pk[i][e] = zero_row ? 0u : pack_bf16x2(lo, hi);
+          }
+        } else if (i < nch) {
+          // two accumulators: the chunk in two 16-column halves (registers:
+          // the second accumulator's half rides along)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[16];
